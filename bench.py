@@ -1,0 +1,453 @@
+"""Benchmark of the tree-verify hot path on one GB300 (or N replicas under torchrun).
+
+One step = tree_build + tree_attention + tree_accept over one batch of a synthetic
+Llama-shaped workload (inputs resident in HBM).  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: effective HBM TB/s of the step = algorithmic bytes (each input byte read once, each
+output byte written once) / step time; also tree nodes verified per second.  The L2 cache
+(129 MB) is flushed by writing a 512 MB buffer before every timed step, outside the timed
+events.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload (the slow plain reference this project is checked against).
+"""
+from __future__ import annotations
+
+import os
+
+# numpy's BLAS threads for the CPU oracle leg: every host core, set before numpy loads
+_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import workloads
+
+DEFAULT_WORKLOAD = "llama2_7b"
+METRIC = "tree-verify effective HBM TB/s (% of GB300 peak) and tree nodes verified/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic bytes
+# ------------------------------------------------------------------------------------
+def algo_bytes(w, prefix_len):
+    s = 4 if w.dtype == "f32" else 2
+    W = (w.m + 63) // 64
+    B, m = w.B, w.m
+    build = B * w.rows * w.V * 4 + B * 4 + B * m * (4 * 3 + 8 * W + 8)
+    kv = sum((int(L) + m) * w.Hkv * w.d * s * 2 for L in prefix_len)
+    blocks = sum(math.ceil((int(L) + m) / workloads.BLOCK_SIZE) for L in prefix_len) * 4
+    attn = 2 * B * m * w.Hq * w.d * s + kv + B * m * W * 8 + blocks + B * 4 + B * m * w.Hq * 4
+    accept = B * m * w.V * s + B * m * 4 * 2 + B * m * 4 * 2 + B * 4 * 2
+    return dict(tree_build=build, tree_attention=attn, tree_accept=accept, step=build + attn + accept)
+
+
+def attention_flops(w, prefix_len):
+    return 4 * w.d * w.Hq * w.m * sum(int(L) for L in prefix_len)
+
+
+# ------------------------------------------------------------------------------------
+# peaks, clocks, traffic
+# ------------------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_eagle_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from a committed ncu summary, or None
+    if there is none for this workload or the kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return e["tree_attention_dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+class Step:
+    """Device buffers + outputs for one verify step of workload w (no allocation per step)."""
+
+    def __init__(self, w, inp, dev):
+        import speculative_decoding_tree_eagle_gb300 as ts
+        self.ts, self.w, self.dev = ts, w, dev
+        self.host = inp
+        self.d = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v) and v.dim() > 0}
+        B, m, W = w.B, w.m, (w.m + 63) // 64
+        self.tree = dict(tokens=torch.empty(B, m, dtype=torch.int32, device=dev),
+                         parents=torch.empty(B, m, dtype=torch.int32, device=dev),
+                         depth=torch.empty(B, m, dtype=torch.int32, device=dev),
+                         mask=torch.empty(B, m, W, dtype=torch.int64, device=dev),
+                         values=torch.empty(B, m, dtype=torch.float64, device=dev))
+        self.out = torch.empty_like(self.d["q"])
+        self.lse = torch.empty(B, m, w.Hq, dtype=torch.float32, device=dev)
+        self.acc = dict(argmax=torch.empty(B, m, dtype=torch.int32, device=dev),
+                        accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                        accept_path=torch.empty(B, m, dtype=torch.int32, device=dev),
+                        bonus=torch.empty(B, dtype=torch.int32, device=dev))
+        dt = self.d["q"].dtype
+        self.ws = [torch.empty(max(n, 256), dtype=torch.uint8, device=dev) for n in (
+            ts.tree_build_workspace(B, w.V, w.k, w.depth, m),
+            ts.tree_attention_workspace(dt, B, m, w.Hq, w.Hkv, w.d, w.max_prefix),
+            ts.tree_accept_workspace(dt, B, m, w.V))]
+        self.status = ts.new_status(dev)
+
+    def build(self):
+        self.ts.tree_build(self.d["draft_logp"], self.d["root_tokens"], self.w.k, self.w.depth, self.w.m,
+                           out=self.tree, workspace=self.ws[0], status=self.status)
+
+    def attention(self):
+        d = self.d
+        self.ts.tree_attention(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["prefix_len"],
+                               self.tree["mask"], max_prefix=self.w.max_prefix, out=self.out, lse=self.lse,
+                               workspace=self.ws[1], status=self.status)
+
+    def accept(self):
+        self.ts.tree_accept(self.d["logits"], self.tree["tokens"], self.tree["parents"], out=self.acc,
+                            workspace=self.ws[2], status=self.status)
+
+    def run(self):
+        self.build()
+        self.attention()
+        self.accept()
+
+
+def run_ours(args, rank, world, dev):
+    import speculative_decoding_tree_eagle_gb300 as ts
+    from speculative_decoding_tree_eagle_gb300 import build as tsbuild
+    tsbuild.build()
+    ts.library()
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.generate(w)
+    step = Step(w, inp, dev)
+    if w.plant_frac > 0:
+        # the planting recipe needs the draft tree: take it from this library's own tree_build
+        step.build()
+        torch.cuda.synchronize()
+        inp["logits"] = workloads.plant_paths(w, inp["logits"], step.tree["tokens"].cpu(),
+                                              step.tree["parents"].cpu())
+        step.d["logits"].copy_(inp["logits"])
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    ts.check_status(step.status)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    t_wall0 = time.time()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = ts.launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        e = evs[i]
+        e[0].record(stream)
+        step.build()
+        e[1].record(stream)
+        step.attention()
+        e[2].record(stream)
+        step.accept()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    launches = ts.launch_count() - n0
+    barrier(world)
+    # keep the GPU busy for at least ~1.5 s overall so the clock sampler sees the load
+    while time.time() - t_wall0 < 1.5:
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ts.check_status(step.status)
+
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_build = [e[0].elapsed_time(e[1]) for e in evs]
+    t_attn = [e[1].elapsed_time(e[2]) for e in evs]
+    t_acc = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(t_step)
+    total_ms = allreduce_max(total_ms, world, dev)
+    ab = algo_bytes(w, inp["prefix_len"].tolist())
+    ms = total_ms / args.steps
+    value = world * ab["step"] / (ms * 1e-3) / 1e12
+    peak, peak_kind = hbm_peak()
+    mean = lambda x: sum(x) / len(x)
+    attn_ms = mean(t_attn)
+    achieved_gbs = ab["tree_attention"] / (attn_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    res = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
+                   "prefix": list(w.prefix), "tree_nodes": w.m, "top_k": w.k, "depth": w.depth, "vocab": w.V,
+                   "block_size": workloads.BLOCK_SIZE, "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replicas{world}"},
+        "pct_of_hbm_peak": round(100 * value * 1e3 / peak, 2),
+        "nodes_verified_per_s": round(world * w.B * w.m / (ms * 1e-3), 1),
+        "nodes_verified_per_s_attention_accept": round(world * w.B * w.m / ((attn_ms + mean(t_acc)) * 1e-3), 1),
+        "kernels_ms": {"tree_build": round(mean(t_build), 5), "tree_attention": round(attn_ms, 5),
+                       "tree_accept": round(mean(t_acc), 5)},
+        "kernels_tbs": {k: round(ab[k] / (mean(t) * 1e-3) / 1e12, 4) for k, t in
+                        (("tree_build", t_build), ("tree_attention", t_attn), ("tree_accept", t_acc))},
+        "algorithmic_bytes": ab,
+        "attention_tflops": round(attention_flops(w, inp["prefix_len"].tolist()) / (attn_ms * 1e-3) / 1e12, 2),
+        "clocks": clocks,
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "kernel": "tree_attention (tcgen05 kernel + split-K combine)",
+                     "achieved": round(achieved_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved_gbs / peak, 4), "traffic": traffic},
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(step, w, ab, args, dev, world)
+    return res, w, inp
+
+
+def run_e2e(step, w, ab, args, dev, world):
+    """Same metric through the public API with host buffers: every step copies its inputs
+    from pinned host memory and reads the tree + acceptance result back."""
+    names = ["draft_logp", "root_tokens", "q", "k_cache", "v_cache", "block_table", "prefix_len", "logits"]
+    host = {n: step.host[n].pin_memory() for n in names}
+    outs = {"tokens": step.tree["tokens"], "parents": step.tree["parents"], "accept_len": step.acc["accept_len"],
+            "accept_path": step.acc["accept_path"], "bonus": step.acc["bonus"]}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for n in names:
+            step.d[n].copy_(host[n], non_blocking=True)
+        step.run()
+        for n, t in outs.items():
+            host_out[n].copy_(t, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            times.append(a.elapsed_time(b))
+    total = allreduce_max(sum(times), world, dev)
+    ms = total / args.steps
+    return {"value": round(world * ab["step"] / (ms * 1e-3) / 1e12, 4), "unit": "TB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle (reported baseline / reference arm)
+# ------------------------------------------------------------------------------------
+def oracle_sample_step(w, inp, heads):
+    """One bounded sample of the step on the fp64 oracle: the whole tree_build and
+    tree_accept, and tree_attention for ``heads`` query heads of every sequence."""
+    import oracle
+    tr = oracle.tree_build(inp["draft_logp"].numpy(), inp["root_tokens"].numpy(), w.k, w.depth, w.m)
+    sel = [(b, i, h) for b in range(w.B) for i in range(w.m) for h in heads]
+    oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
+                          inp["prefix_len"].numpy(), tr["mask"], 1.0 / math.sqrt(w.d), select=sel)
+    amax = oracle.target_argmax(inp["logits"])
+    oracle.accept_longest_path(tr["tokens"], tr["parents"], amax)
+
+
+def oracle_sample_bytes(w, ab, heads):
+    frac = len(heads) / w.Hq
+    return ab["tree_build"] + ab["tree_attention"] * frac + ab["tree_accept"]
+
+
+def pick_heads(w):
+    g = w.Hq // w.Hkv
+    n = max(1, min(w.Hq, 4))
+    return [h * g % w.Hq for h in range(n)] if g > 1 else list(range(n))
+
+
+def cpu_baseline(w, inp, budget_s=12.0):
+    ab = algo_bytes(w, inp["prefix_len"].tolist())
+    heads = pick_heads(w)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_sample_step(w, inp, heads)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    byts = oracle_sample_bytes(w, ab, heads)
+    return {"value": round(byts / dt / 1e12, 8), "unit": "TB/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"fp64 numpy oracle: full tree_build + tree_accept, tree_attention for {len(heads)} of "
+                      f"{w.Hq} query heads (all sequences and nodes); {n} repetitions, {dt:.3f} s each; "
+                      f"metric scaled by the sample's algorithmic bytes"}
+
+
+def run_reference(args, rank, world):
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.generate(w)
+    ab = algo_bytes(w, inp["prefix_len"].tolist())
+    heads = pick_heads(w)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, inp, heads)
+    ts_ = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample_step(w, inp, heads)
+        ts_.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(ts_) / len(ts_)
+    byts = oracle_sample_bytes(w, ab, heads)
+    value = byts / (ms * 1e-3) / 1e12
+    sample = (f"fp64 numpy oracle: full tree_build + tree_accept, tree_attention for {len(heads)} of {w.Hq} "
+              f"query heads; metric scaled by the sample's algorithmic bytes")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "TB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
+                       "prefix": list(w.prefix), "tree_nodes": w.m, "vocab": w.V},
+            "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": _CORES, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 8), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ------------------------------------------------------------------------------------
+_PG = None
+
+
+def init_dist(args):
+    global _PG
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        _PG = dist
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1 and _PG is not None:
+        _PG.barrier()
+
+
+def allreduce_max(x, world, dev):
+    if world <= 1 or _PG is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev if _PG.get_backend() == "nccl" else "cpu")
+    _PG.all_reduce(t, op=_PG.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    rank, world, local = init_dist(args)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    res, w, inp = run_ours(args, rank, world, dev)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(w, inp)
+        print(json.dumps(res), flush=True)
+    if world > 1 and _PG is not None:
+        _PG.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * treespec.h — C ABI of libtreespec.so: the tree-verify hot path of EAGLE-2-style
+ * speculative decoding on one GB300 (sm_103a).
+ *
+ * Three operations, each a set of hand-written CUDA kernels:
+ *   ts_tree_build      dynamic draft-tree construction (expand, rerank, flatten, mask)
+ *   ts_tree_attention  every tree node attends to the paged KV prefix + its own ancestors
+ *   ts_tree_accept     per-node argmax of the target logits + longest matching root path
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer owned by the caller.  The library never
+ *     allocates device memory; scratch space is the caller's `workspace`, sized by the
+ *     matching *_workspace() query (any contents on entry; not zeroed by the caller).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns after the launches are queued.
+ *   - Arguments are validated on the host before anything is launched: bad sizes or null
+ *     pointers return TS_ERR_INVALID, sizes outside the supported range return
+ *     TS_ERR_UNSUPPORTED, a too-small workspace returns TS_ERR_WORKSPACE.  Nothing is
+ *     launched in those cases.  A failed launch returns TS_ERR_CUDA.
+ *   - Problems the host cannot see (a block id out of range, a parent index that does
+ *     not precede its child, a prefix length above `max_prefix`, a bounded wait that
+ *     timed out) are reported on the device: the first such error code is stored into
+ *     `*dev_status` (an int32 device word, may be NULL to ignore) and the affected work is
+ *     skipped.  Kernels never trap.  The caller zeroes *dev_status and reads it after the
+ *     stream has synchronised.
+ *   - The library keeps no state between calls and is safe to call from several host
+ *     threads.  Calls that share a workspace must be ordered on one stream.
+ *
+ * Notation: B sequences, m tree nodes per sequence INCLUDING the root (node 0), k draft
+ * top-k, depth draft layers below the root, V vocabulary, Hq query heads, Hkv KV heads
+ * (Hq % Hkv == 0, g = Hq / Hkv), d head dim, W = ceil(m / 64) mask words per node.
+ */
+#ifndef TREESPEC_H
+#define TREESPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID = -1,       /* null pointer, non-positive size, inconsistent sizes */
+  TS_ERR_UNSUPPORTED = -2,   /* valid but outside the supported range (limits below) */
+  TS_ERR_WORKSPACE = -3,     /* workspace smaller than the *_workspace() query */
+  TS_ERR_CUDA = -4,          /* a CUDA launch or driver call failed */
+  TS_ERR_TIMEOUT = -5,       /* device: a bounded wait gave up (written to *dev_status) */
+  TS_ERR_DEVICE_CHECK = -6   /* device: bad data found in an input (written to *dev_status) */
+} ts_status;
+
+typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
+
+/* Limits (host-checked).  m <= TS_MAX_NODES, k <= TS_MAX_TOPK, depth <= TS_MAX_DEPTH. */
+#define TS_MAX_NODES 256
+#define TS_MAX_TOPK 16
+#define TS_MAX_DEPTH 16
+
+/* Human-readable name of a ts_status value (static string, never NULL). */
+const char* ts_status_string(int status);
+
+/* Library ABI version (this header describes version 1). */
+int ts_version(void);
+
+/* Total number of CUDA kernels this process has launched through the library so far
+ * (monotonic, thread-safe; a diagnostic for counting launches around a timed region). */
+uint64_t ts_launch_count(void);
+
+/* ------------------------------------------------------------------------------------
+ * ts_tree_build — EAGLE-2 dynamic draft tree.
+ * Source: "rainlin.net/posts/eagle" (EAGLE series), section 7.1 Expansion (expand the top-k
+ * nodes of the deepest layer by global acceptance value = product of the draft confidences
+ * on the root path, kept here as a sum of log-probabilities), section 7.2 Reranking (top-m
+ * of all nodes, shallower first, still a connected tree; flatten; build the mask), section 四
+ * (each node sees exactly its root-to-node path); "lesty.tech — EAGLE-2 vs. Medusa",
+ * section 5 (the mask from the parent array).
+ *
+ * draft_logp  [B, R, V] fp32, R = 1 + (depth-1)*k, row-major.  Draft log-probabilities
+ *             (<= 0).  Row 0 is the root's next-token distribution; row 1 + (l-2)*k + j is
+ *             the distribution after the j-th selected frontier node of layer l-1 (frontier
+ *             slots in order of value, highest first).  Read only.
+ * root_tokens [B] int32: token of node 0 (the last committed token).
+ * k, depth, m 1 <= k <= 16, 1 <= depth <= 16, 1 <= m <= 256, m - 1 <= k + (depth-1)*k*k.
+ * Outputs ([B, m] row-major unless stated):
+ *   tokens    int32 token of each flattened node (node 0 = root).
+ *   parents   int32 flat index of the parent, -1 for the root; parents precede children.
+ *   depth_out int32 depth below the root (root 0).
+ *   mask      uint64 [B, m, W]: bit (j % 64) of word j / 64 of row i is set iff node j is
+ *             node i or one of its ancestors.
+ *   values    fp64 (optional, NULL to skip): global value = summed log-probs, root 0.
+ * Order of the flattened nodes: root, then by (depth, parent's flat index, rank of the
+ * child within its parent's top-k).  Top-k ties -> lower token id; frontier ties -> lower
+ * layer-local index; rerank ties -> shallower, then lower layer-local index.
+ * Device errors: a selection that is not a connected tree (possible only if some
+ * log-prob > 0) -> TS_ERR_DEVICE_CHECK for that sequence.
+ * --------------------------------------------------------------------------------- */
+size_t ts_tree_build_workspace(int B, int V, int k, int depth, int m);
+int ts_tree_build(const float* draft_logp, const int32_t* root_tokens,
+                  int B, int V, int k, int depth, int m,
+                  int32_t* tokens, int32_t* parents, int32_t* depth_out, uint64_t* mask,
+                  double* values,
+                  void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * ts_tree_attention — tree attention over a paged KV cache, batched, GQA.
+ * Source: "rainlin.net/posts/eagle", section 四 Tree Attention (the flattened tree is fed in
+ * one pass; node i attends only to its root-to-node ancestors, which equals verifying
+ * every path separately); "lesty.tech — EAGLE-2 vs. Medusa", section 5 (mask held on chip,
+ * no re-reads) and section 8 (the tree's K/V sit in blocks of the same paged sequence,
+ * after the committed prefix).
+ *
+ * For sequence b, query head h (KV head h / g) and node i:
+ *   keys = prefix positions 0..L_b-1  U  { L_b + t : mask bit t of row i is set }
+ *   out  = softmax(scale * q . k^T) . v over those keys,  lse = log of the softmax sum
+ * q          [B, m, Hq, d]  (dt: fp32 or bf16), 16-byte aligned.
+ * k_cache,
+ * v_cache    [num_blocks, Hkv, block_size, d] (dt), 16-byte aligned.  Logical position p
+ *            of sequence b lives in block block_table[b*max_blocks + p/block_size], row
+ *            p % block_size.  Positions L_b .. L_b+m-1 hold the tree nodes' K/V (already
+ *            written by the caller, with whatever positional encoding it applies).
+ * block_table [B, max_blocks] int32; entries for positions >= L_b + m are not read.
+ * prefix_len [B] int32, 0 <= L_b <= max_prefix, and L_b + m <= max_blocks*block_size.
+ * max_prefix host-side upper bound of prefix_len (sizes the launch and the workspace).
+ * mask       [B, m, W] uint64 as produced by ts_tree_build.
+ * scale      softmax scale (normally 1/sqrt(d)).
+ * out        [B, m, Hq, d] (dt).  lse: [B, m, Hq] fp32 natural-log sum-exp (NULL ok).
+ * Supported: fp32 any d <= 256 (CUDA-core path, fp32 accumulation); bf16 with d == 128
+ * and block_size in {16, 32, 64, 128} (tcgen05 tensor-core path, TMA-staged K/V, fp32
+ * accumulation, P rounded to bf16 for the PV product).  m <= 256.
+ * Device errors: block id outside [0, num_blocks) or prefix_len outside [0, max_prefix]
+ * -> TS_ERR_DEVICE_CHECK; a pipeline wait that exceeded its time bound -> TS_ERR_TIMEOUT.
+ * --------------------------------------------------------------------------------- */
+size_t ts_tree_attention_workspace(ts_dtype dt, int B, int m, int Hq, int Hkv, int d,
+                                   int max_prefix);
+int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, ts_dtype dt,
+                      int num_blocks, int block_size, const int32_t* block_table,
+                      int max_blocks, const int32_t* prefix_len, int max_prefix,
+                      const uint64_t* mask, int B, int m, int Hq, int Hkv, int d,
+                      float scale, void* out, float* lse,
+                      void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * ts_tree_accept — greedy verification of the tree.
+ * Source: "lesty.tech — EAGLE-2 vs. Medusa", section 4 (greedy: a draft token is accepted iff
+ * it is the base model's argmax given its context, here its parent's position);
+ * "rainlin.net/posts/eagle", section 3.2 (accept the longest valid branch).
+ *
+ * logits     [B, m, V] (dt), row (b, i) = target distribution after node i's root path.
+ * tokens, parents [B, m] int32 (as from ts_tree_build; parents precede children).
+ * Outputs:
+ *   argmax      [B, m] int32, first index of the row maximum (ties -> lowest id).
+ *   accept_len  [B] int32 >= 1: nodes on the accepted path, root included.
+ *   accept_path [B, m] int32: flat indices root..accepted node, then -1.
+ *   bonus       [B] int32: argmax at the accepted node (the token the step emits after
+ *               the accepted drafts).
+ * A node is valid when every non-root node on its root path has token == argmax of its
+ * parent.  The accepted node is the deepest valid node, ties -> lowest flat index.
+ * Device errors: parents[0] != -1 or parents[i] not in [0, i) -> TS_ERR_DEVICE_CHECK, and
+ * that sequence's outputs are accept_len 0, path all -1, bonus -1.
+ * --------------------------------------------------------------------------------- */
+size_t ts_tree_accept_workspace(ts_dtype dt, int B, int m, int V);
+int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
+                   const int32_t* parents, int B, int m, int V,
+                   int32_t* argmax, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
+                   void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREESPEC_H */

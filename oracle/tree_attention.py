@@ -36,14 +36,21 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def gather_sequence(cache: np.ndarray, table_row: np.ndarray, n: int) -> np.ndarray:
-    """Logical positions 0..n-1 of one sequence from a paged cache -> [n, Hkv, d]."""
+def gather_sequence(cache, table_row, n: int) -> np.ndarray:
+    """Logical positions 0..n-1 of one sequence from a paged cache -> fp64 [n, Hkv, d].
+
+    Only the gathered rows are widened to fp64 (exactly), so large caches stay in their
+    storage type."""
     bs = cache.shape[2]
     pos = np.arange(n)
     blocks = np.asarray(table_row)[pos // bs]
     if np.any(blocks < 0) or np.any(blocks >= cache.shape[0]):
         raise ValueError("block table entry out of range")
-    return cache[blocks, :, pos % bs, :]
+    if hasattr(cache, "detach"):
+        import torch
+        rows = cache[torch.from_numpy(blocks), :, torch.from_numpy(pos % bs), :]
+        return _f64(rows)
+    return np.asarray(cache[blocks, :, pos % bs, :], dtype=np.float64)
 
 
 def tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale: float,
@@ -56,8 +63,7 @@ def tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale: fl
     Returns (out [B, m, Hq, d] fp64, lse [B, m, Hq] fp64); unselected entries are NaN.
     """
     qd = _f64(q)
-    kc = _f64(k_cache)
-    vc = _f64(v_cache)
+    kc, vc = k_cache, v_cache
     table = np.asarray(block_table).astype(np.int64)
     plen = np.asarray(prefix_len).astype(np.int64)
     mask = np.asarray(mask, dtype=bool)

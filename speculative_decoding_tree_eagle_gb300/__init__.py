@@ -1,0 +1,243 @@
+"""GB300 tree-verify hot path for EAGLE-2-style speculative decoding (Python binding).
+
+Thin ctypes binding over ``libtreespec.so`` (C ABI in ``include/treespec.h``).  The
+functions below only check tensor metadata, allocate outputs with torch and pass raw
+device pointers plus torch's current CUDA stream; every step of the computation runs in
+the library's CUDA kernels.  There is no CPU fallback: without the built library, or
+without a CUDA device, every call raises.
+
+    tree_build(draft_logp, root_tokens, k, depth, m)      -> dict(tokens, parents, depth, mask, values)
+    tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, ...) -> (out, lse)
+    tree_accept(logits, tokens, parents)                  -> dict(argmax, accept_len, accept_path, bonus)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Dict, Optional
+
+import torch
+
+__all__ = [
+    "TreeSpecError", "library", "library_path", "launch_count", "status_string",
+    "tree_build", "tree_attention", "tree_accept", "new_status", "check_status",
+    "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libtreespec.so")
+
+TS_F32, TS_BF16 = 0, 1
+_lib = None
+_lock = threading.Lock()
+
+
+class TreeSpecError(RuntimeError):
+    pass
+
+
+def library():
+    """Load libtreespec.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(library_path):
+            raise TreeSpecError(f"{library_path} is missing: build it with "
+                                "`python -m speculative_decoding_tree_eagle_gb300.build`")
+        L = ctypes.CDLL(library_path)
+        P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        L.ts_status_string.restype = ctypes.c_char_p
+        L.ts_status_string.argtypes = [I]
+        L.ts_version.restype = I
+        L.ts_launch_count.restype = ctypes.c_uint64
+        L.ts_tree_build_workspace.restype = S
+        L.ts_tree_build_workspace.argtypes = [I, I, I, I, I]
+        L.ts_tree_build.restype = I
+        L.ts_tree_build.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P, S, P, P]
+        L.ts_tree_attention_workspace.restype = S
+        L.ts_tree_attention_workspace.argtypes = [I, I, I, I, I, I, I]
+        L.ts_tree_attention.restype = I
+        L.ts_tree_attention.argtypes = [P, P, P, I, I, I, P, I, P, I, P, I, I, I, I, I, F, P, P, P, S, P, P]
+        L.ts_tree_accept_workspace.restype = S
+        L.ts_tree_accept_workspace.argtypes = [I, I, I, I]
+        L.ts_tree_accept.restype = I
+        L.ts_tree_accept.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, S, P, P]
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return library().ts_status_string(int(code)).decode()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(library().ts_launch_count())
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise TreeSpecError(status_string(rc))
+
+
+def _p(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TS_F32
+    if t.dtype == torch.bfloat16:
+        return TS_BF16
+    raise ValueError(f"unsupported dtype {t.dtype} (fp32 or bf16)")
+
+
+_ws_cache: Dict[int, torch.Tensor] = {}
+
+
+def _workspace(nbytes: int, device: torch.device, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return ws
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    cur = _ws_cache.get(idx)
+    if cur is None or cur.numel() < nbytes:
+        cur = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[idx] = cur
+    return cur
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed int32 device word for the kernels' device-side error codes."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(status: torch.Tensor) -> None:
+    """Synchronise and raise if a kernel reported a device-side error."""
+    code = int(status.item())
+    if code != 0:
+        raise TreeSpecError(status_string(code))
+
+
+def tree_build_workspace(B: int, V: int, k: int, depth: int, m: int) -> int:
+    return int(library().ts_tree_build_workspace(B, V, k, depth, m))
+
+
+def tree_attention_workspace(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: int, d: int,
+                             max_prefix: int) -> int:
+    dt = TS_F32 if dtype == torch.float32 else TS_BF16
+    return int(library().ts_tree_attention_workspace(dt, B, m, Hq, Hkv, d, max_prefix))
+
+
+def tree_accept_workspace(dtype: torch.dtype, B: int, m: int, V: int) -> int:
+    dt = TS_F32 if dtype == torch.float32 else TS_BF16
+    return int(library().ts_tree_accept_workspace(dt, B, m, V))
+
+
+def tree_build(draft_logp: torch.Tensor, root_tokens: torch.Tensor, k: int, depth: int, m: int, *,
+               out: Optional[Dict[str, torch.Tensor]] = None, with_values: bool = True,
+               workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """EAGLE-2 dynamic draft tree: draft_logp [B, 1+(depth-1)k, V] fp32 log-probs, root_tokens [B] int32."""
+    L = library()
+    _need_cuda("draft_logp", draft_logp, torch.float32)
+    _need_cuda("root_tokens", root_tokens, torch.int32)
+    B, R, V = draft_logp.shape
+    if R != 1 + (depth - 1) * k:
+        raise ValueError(f"draft_logp must have {1 + (depth - 1) * k} rows per sequence, got {R}")
+    dev = draft_logp.device
+    W = (m + 63) // 64
+    if out is None:
+        out = dict(tokens=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   parents=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   depth=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   mask=torch.empty(B, m, W, dtype=torch.int64, device=dev))
+        if with_values:
+            out["values"] = torch.empty(B, m, dtype=torch.float64, device=dev)
+    need = L.ts_tree_build_workspace(B, V, k, depth, m)
+    if need == 0:
+        raise TreeSpecError("invalid tree_build sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_tree_build(_p(draft_logp), _p(root_tokens), B, V, k, depth, m, _p(out["tokens"]),
+                           _p(out["parents"]), _p(out["depth"]), _p(out["mask"]), _p(out.get("values")),
+                           _p(ws), ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                   prefix_len: torch.Tensor, mask: torch.Tensor, *, max_prefix: int,
+                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+                   workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Tree attention.  q [B,m,Hq,d]; caches [num_blocks,Hkv,block_size,d]; block_table [B,max_blocks]
+    int32; prefix_len [B] int32; mask [B,m,ceil(m/64)] (int64 view of uint64 words)."""
+    L = library()
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("prefix_len", prefix_len, torch.int32)
+    _need_cuda("mask", mask, torch.int64)
+    B, m, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if mask.shape != (B, m, (m + 63) // 64):
+        raise ValueError("mask must be [B, m, ceil(m/64)]")
+    dt = _dt(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty(B, m, Hq, dtype=torch.float32, device=q.device)
+    need = L.ts_tree_attention_workspace(dt, B, m, Hq, Hkv, d, max_prefix)
+    ws = _workspace(max(need, 256), q.device, workspace)
+    _check(L.ts_tree_attention(_p(q), _p(k_cache), _p(v_cache), dt, NB, bs, _p(block_table),
+                               block_table.shape[1], _p(prefix_len), int(max_prefix), _p(mask), B, m, Hq,
+                               Hkv, d, float(scale), _p(out), _p(lse), _p(ws),
+                               ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out, lse
+
+
+def tree_accept(logits: torch.Tensor, tokens: torch.Tensor, parents: torch.Tensor, *,
+                out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """Per-node argmax of logits [B,m,V] and the longest matching root path."""
+    L = library()
+    _need_cuda("logits", logits)
+    _need_cuda("tokens", tokens, torch.int32)
+    _need_cuda("parents", parents, torch.int32)
+    B, m, V = logits.shape
+    dt = _dt(logits)
+    dev = logits.device
+    if out is None:
+        out = dict(argmax=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   accept_path=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   bonus=torch.empty(B, dtype=torch.int32, device=dev))
+    need = L.ts_tree_accept_workspace(dt, B, m, V)
+    if need == 0:
+        raise TreeSpecError("invalid tree_accept sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_tree_accept(_p(logits), dt, _p(tokens), _p(parents), B, m, V, _p(out["argmax"]),
+                            _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws),
+                            ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out

@@ -1,0 +1,155 @@
+// C ABI of libtreespec.so (declared in include/treespec.h): host-side argument validation,
+// workspace sizing and dispatch to the kernels.  Nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_build(int B, int V, int k, int depth, int m) {
+  if (B <= 0 || V <= 0 || k <= 0 || depth <= 0 || m <= 0) return TS_ERR_INVALID;
+  if (k > TS_MAX_TOPK || depth > TS_MAX_DEPTH || m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
+  if (k > V) return TS_ERR_INVALID;
+  const long long ncand = k + static_cast<long long>(depth - 1) * k * k;
+  if (m - 1 > ncand) return TS_ERR_INVALID;
+  const long long R = 1 + static_cast<long long>(depth - 1) * k;
+  if (static_cast<long long>(B) * R * V > (1LL << 40)) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+static int check_attention(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix) {
+  if (B <= 0 || m <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_prefix < 0) return TS_ERR_INVALID;
+  if (dt != TS_F32 && dt != TS_BF16) return TS_ERR_INVALID;
+  if (Hq % Hkv != 0) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES || d > 256 || static_cast<long long>(B) * Hkv > 65535)
+    return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+static int check_accept(ts_dtype dt, int B, int m, int V) {
+  if (B <= 0 || m <= 0 || V <= 0) return TS_ERR_INVALID;
+  if (dt != TS_F32 && dt != TS_BF16) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+}  // namespace ts
+
+extern "C" {
+
+const char* ts_status_string(int status) {
+  switch (status) {
+    case TS_OK: return "TS_OK";
+    case TS_ERR_INVALID: return "TS_ERR_INVALID: invalid argument";
+    case TS_ERR_UNSUPPORTED: return "TS_ERR_UNSUPPORTED: size outside the supported range";
+    case TS_ERR_WORKSPACE: return "TS_ERR_WORKSPACE: workspace too small";
+    case TS_ERR_CUDA: return "TS_ERR_CUDA: CUDA launch or driver call failed";
+    case TS_ERR_TIMEOUT: return "TS_ERR_TIMEOUT: a bounded device wait timed out";
+    case TS_ERR_DEVICE_CHECK: return "TS_ERR_DEVICE_CHECK: bad input data found on the device";
+    default: return "unknown ts_status";
+  }
+}
+
+int ts_version(void) { return 1; }
+
+uint64_t ts_launch_count(void) { return ts::g_launches.load(std::memory_order_relaxed); }
+
+size_t ts_tree_build_workspace(int B, int V, int k, int depth, int m) {
+  if (ts::check_build(B, V, k, depth, m) != TS_OK) return 0;
+  return ts::tree_build_workspace_bytes(B, V, k, depth, ts::device_sm_count());
+}
+
+int ts_tree_build(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
+                  int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
+                  uint64_t* mask, double* values, void* workspace, size_t ws_bytes,
+                  int32_t* dev_status, void* stream) {
+  const int rc = ts::check_build(B, V, k, depth, m);
+  if (rc != TS_OK) return rc;
+  if (!draft_logp || !root_tokens || !tokens || !parents || !depth_out || !mask || !workspace)
+    return TS_ERR_INVALID;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  if (ws_bytes < ts::tree_build_workspace_bytes(B, V, k, depth, sms)) return TS_ERR_WORKSPACE;
+  return ts::tree_build_launch(draft_logp, root_tokens, B, V, k, depth, m, tokens, parents,
+                               depth_out, mask, values, workspace, dev_status,
+                               static_cast<cudaStream_t>(stream), sms);
+}
+
+size_t ts_tree_attention_workspace(ts_dtype dt, int B, int m, int Hq, int Hkv, int d,
+                                   int max_prefix) {
+  if (ts::check_attention(dt, B, m, Hq, Hkv, d, max_prefix) != TS_OK) return 0;
+  // the tensor-core path with the common 16-row pages; other page sizes plan the same
+  if (ts::attention_uses_tc(dt, d, 16))
+    return ts::attention_tc_workspace_bytes(B, m, Hq, Hkv, max_prefix, ts::device_sm_count());
+  return 256;
+}
+
+int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, ts_dtype dt,
+                      int num_blocks, int block_size, const int32_t* block_table,
+                      int max_blocks, const int32_t* prefix_len, int max_prefix,
+                      const uint64_t* mask, int B, int m, int Hq, int Hkv, int d,
+                      float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      int32_t* dev_status, void* stream) {
+  int rc = ts::check_attention(dt, B, m, Hq, Hkv, d, max_prefix);
+  if (rc != TS_OK) return rc;
+  if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !mask || !out)
+    return TS_ERR_INVALID;
+  if (num_blocks <= 0 || block_size <= 0 || max_blocks <= 0 || !std::isfinite(scale))
+    return TS_ERR_INVALID;
+  if (static_cast<long long>(max_blocks) * block_size < static_cast<long long>(max_prefix) + m)
+    return TS_ERR_INVALID;
+  ts::AttnArgs a{q, k_cache, v_cache, dt, num_blocks, block_size, block_table, max_blocks,
+                 prefix_len, max_prefix, mask, B, m, Hq, Hkv, d, scale, out, lse, workspace,
+                 dev_status, static_cast<cudaStream_t>(stream)};
+  if (ts::attention_uses_tc(dt, d, block_size)) {
+    if (!ts::aligned16(q) || !ts::aligned16(k_cache) || !ts::aligned16(v_cache) || !ts::aligned16(out))
+      return TS_ERR_INVALID;
+    const int sms = ts::device_sm_count();
+    if (sms <= 0) return TS_ERR_CUDA;
+    const size_t need = ts::attention_tc_workspace_bytes(B, m, Hq, Hkv, max_prefix, sms);
+    if (need > 256 && (!workspace || ws_bytes < need)) return TS_ERR_WORKSPACE;
+    if (!ts::aligned16(workspace) && need > 256) return TS_ERR_INVALID;
+    return ts::attention_tc_launch(a, sms);
+  }
+  return ts::attention_simt_launch(a);
+}
+
+size_t ts_tree_accept_workspace(ts_dtype dt, int B, int m, int V) {
+  if (ts::check_accept(dt, B, m, V) != TS_OK) return 0;
+  return ts::tree_accept_workspace_bytes(dt, B, m, V, ts::device_sm_count());
+}
+
+int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
+                   const int32_t* parents, int B, int m, int V, int32_t* argmax,
+                   int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
+                   size_t ws_bytes, int32_t* dev_status, void* stream) {
+  const int rc = ts::check_accept(dt, B, m, V);
+  if (rc != TS_OK) return rc;
+  if (!logits || !tokens || !parents || !argmax || !accept_len || !accept_path || !bonus ||
+      !workspace)
+    return TS_ERR_INVALID;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  if (ws_bytes < ts::tree_accept_workspace_bytes(dt, B, m, V, sms)) return TS_ERR_WORKSPACE;
+  return ts::tree_accept_launch(logits, dt, tokens, parents, B, m, V, argmax, accept_len,
+                                accept_path, bonus, workspace, dev_status,
+                                static_cast<cudaStream_t>(stream), sms);
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Internal launch entry points behind the C ABI (host side).  Arguments are already
+// validated by the C-ABI layer when these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "treespec.h"
+
+namespace ts {
+
+int device_sm_count();
+
+size_t tree_build_workspace_bytes(int B, int V, int k, int depth, int num_sms);
+int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
+                      int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
+                      uint64_t* mask, double* values, void* workspace, int32_t* dev_status,
+                      cudaStream_t stream, int num_sms);
+
+size_t tree_accept_workspace_bytes(ts_dtype dt, int B, int m, int V, int num_sms);
+int tree_accept_launch(const void* logits, ts_dtype dt, const int32_t* tokens,
+                       const int32_t* parents, int B, int m, int V, int32_t* argmax,
+                       int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
+                       int32_t* dev_status, cudaStream_t stream, int num_sms);
+
+struct AttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  ts_dtype dt;
+  int num_blocks, block_size;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* prefix_len;
+  int max_prefix;
+  const uint64_t* mask;
+  int B, m, Hq, Hkv, d;
+  float scale;
+  void* out;
+  float* lse;
+  void* workspace;
+  int32_t* dev_status;
+  cudaStream_t stream;
+};
+
+// Whether the tensor-core path handles this shape (bf16, d == 128, block size 16..128).
+bool attention_uses_tc(ts_dtype dt, int d, int block_size);
+size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms);
+int attention_tc_launch(const AttnArgs& a, int num_sms);
+int attention_simt_launch(const AttnArgs& a);
+
+}  // namespace ts

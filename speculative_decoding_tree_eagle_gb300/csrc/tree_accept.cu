@@ -1,0 +1,273 @@
+// ts_tree_accept kernels: greedy verification of the draft tree.
+//
+// Source: "lesty.tech — EAGLE-2 vs. Medusa", section 4 (greedy acceptance: a draft token is
+// kept iff it is the base model's argmax in its context); "rainlin.net/posts/eagle",
+// section 3.2 (the longest valid branch is accepted).
+//
+// Two launches:
+//   1. argmax_kernel — the HBM stream over the [B*m, V] target logits.  Each CTA reduces
+//      one segment of one row with 16-byte loads (4 in flight per thread), a per-thread
+//      running (max, first index), a warp-shuffle and a shared-memory reduction.  Partial
+//      (value, index) pairs go to the workspace.
+//   2. accept_kernel — one CTA per sequence: merge the partials of each node's row, check
+//      the parent array, mark each node valid if every node on its root path carries the
+//      argmax of its parent, pick the deepest valid node (ties -> lowest index) with a
+//      block max over a packed key, and write the path, its length and the bonus token.
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+namespace {
+
+constexpr int kArgThreads = 256;
+constexpr int kAcceptThreads = 256;
+
+__device__ __forceinline__ void upd(float& bv, int& bi, float v, int i) {
+  if (better(v, i, bv, bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
+__device__ __forceinline__ void block_best(float& v, int& i) {
+  __shared__ float s_v[32];
+  __shared__ int s_i[32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    upd(v, i, ov, oi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_v[warp] = v;
+    s_i[warp] = i;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    v = lane < nw ? s_v[lane] : -INFINITY;
+    i = lane < nw ? s_i[lane] : INT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+      upd(v, i, ov, oi);
+    }
+  }
+}
+
+// bf16 rows: 8 values per 16-byte load.
+__global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
+    const __nv_bfloat16* __restrict__ logits, int V, int seg_len, int S, int vec,
+    float* __restrict__ part_v, int* __restrict__ part_i) {
+  const long long row = blockIdx.x / S;
+  const int seg = blockIdx.x % S;
+  const __nv_bfloat16* x = logits + row * static_cast<long long>(V);
+  const int begin = seg * seg_len, end = min(V, begin + seg_len);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  if (vec) {
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    const int b8 = begin >> 3, e8 = end >> 3;
+    int i = b8 + threadIdx.x;
+    for (; i + 3 * kArgThreads < e8; i += 4 * kArgThreads) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = __ldcs(x8 + i + u * kArgThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int base = (i + u * kArgThreads) << 3;
+        upd(bv, bi, bf16_lo(a[u].x), base + 0);
+        upd(bv, bi, bf16_hi(a[u].x), base + 1);
+        upd(bv, bi, bf16_lo(a[u].y), base + 2);
+        upd(bv, bi, bf16_hi(a[u].y), base + 3);
+        upd(bv, bi, bf16_lo(a[u].z), base + 4);
+        upd(bv, bi, bf16_hi(a[u].z), base + 5);
+        upd(bv, bi, bf16_lo(a[u].w), base + 6);
+        upd(bv, bi, bf16_hi(a[u].w), base + 7);
+      }
+    }
+    for (; i < e8; i += kArgThreads) {
+      const uint4 a = __ldcs(x8 + i);
+      const int base = i << 3;
+      upd(bv, bi, bf16_lo(a.x), base + 0);
+      upd(bv, bi, bf16_hi(a.x), base + 1);
+      upd(bv, bi, bf16_lo(a.y), base + 2);
+      upd(bv, bi, bf16_hi(a.y), base + 3);
+      upd(bv, bi, bf16_lo(a.z), base + 4);
+      upd(bv, bi, bf16_hi(a.z), base + 5);
+      upd(bv, bi, bf16_lo(a.w), base + 6);
+      upd(bv, bi, bf16_hi(a.w), base + 7);
+    }
+  } else {
+    const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
+    for (int i = begin + threadIdx.x; i < end; i += kArgThreads)
+      upd(bv, bi, __uint_as_float(static_cast<uint32_t>(xs[i]) << 16), i);
+  }
+  block_best(bv, bi);
+  if (threadIdx.x == 0) {
+    part_v[row * S + seg] = bv;
+    part_i[row * S + seg] = bi;
+  }
+}
+
+__global__ void __launch_bounds__(kArgThreads) argmax_f32_kernel(
+    const float* __restrict__ logits, int V, int seg_len, int S, int vec,
+    float* __restrict__ part_v, int* __restrict__ part_i) {
+  const long long row = blockIdx.x / S;
+  const int seg = blockIdx.x % S;
+  const float* x = logits + row * static_cast<long long>(V);
+  const int begin = seg * seg_len, end = min(V, begin + seg_len);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int i = (begin >> 2) + threadIdx.x; i < (end >> 2); i += kArgThreads) {
+      const float4 a = __ldcs(x4 + i);
+      const int base = i << 2;
+      upd(bv, bi, a.x, base);
+      upd(bv, bi, a.y, base + 1);
+      upd(bv, bi, a.z, base + 2);
+      upd(bv, bi, a.w, base + 3);
+    }
+  } else {
+    for (int i = begin + threadIdx.x; i < end; i += kArgThreads) upd(bv, bi, __ldcs(x + i), i);
+  }
+  block_best(bv, bi);
+  if (threadIdx.x == 0) {
+    part_v[row * S + seg] = bv;
+    part_i[row * S + seg] = bi;
+  }
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
+    const float* __restrict__ part_v, const int* __restrict__ part_i, int S,
+    const int32_t* __restrict__ tokens, const int32_t* __restrict__ parents, int m,
+    int32_t* __restrict__ argmax, int32_t* __restrict__ accept_len,
+    int32_t* __restrict__ accept_path, int32_t* __restrict__ bonus, int32_t* status) {
+  __shared__ int s_amax[TS_MAX_NODES];
+  __shared__ int s_par[TS_MAX_NODES];
+  __shared__ int s_tok[TS_MAX_NODES];
+  __shared__ unsigned s_key[32];
+  const int b = blockIdx.x, i = threadIdx.x;
+  const long long r0 = static_cast<long long>(b) * m;
+  bool bad = false;
+  if (i < m) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int s = 0; s < S; ++s) upd(bv, bi, part_v[(r0 + i) * S + s], part_i[(r0 + i) * S + s]);
+    s_amax[i] = bi;
+    argmax[r0 + i] = bi;
+    const int p = parents[r0 + i];
+    s_par[i] = p;
+    s_tok[i] = tokens[r0 + i];
+    bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+  }
+  if (__syncthreads_or(bad)) {
+    if (i == 0) {
+      report(status, TS_ERR_DEVICE_CHECK);
+      accept_len[b] = 0;
+      bonus[b] = -1;
+    }
+    for (int j = i; j < m; j += blockDim.x) accept_path[r0 + j] = -1;
+    return;
+  }
+  // valid node: every node on the root path carries its parent's argmax token
+  unsigned key = 0u;
+  if (i < m) {
+    int n = i, d = 0;
+    bool ok = true;
+    while (n != 0) {
+      const int p = s_par[n];
+      if (s_tok[n] != s_amax[p]) {
+        ok = false;
+        break;
+      }
+      n = p;
+      ++d;
+    }
+    // deepest first, then lowest index; 0 means "not valid" (the root's key is 0xFFFF)
+    if (ok) key = (static_cast<unsigned>(d) << 16) | (0xFFFFu - static_cast<unsigned>(i));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
+  if ((i & 31) == 0) s_key[i >> 5] = key;
+  __syncthreads();
+  if (i < 32) {
+    key = (i < static_cast<int>(blockDim.x >> 5)) ? s_key[i] : 0u;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
+    if (i == 0) s_key[0] = key;
+  }
+  __syncthreads();
+  key = s_key[0];
+  const int best = static_cast<int>(0xFFFFu - (key & 0xFFFFu));
+  const int dbest = static_cast<int>(key >> 16);
+  for (int j = dbest + 1 + i; j < m; j += blockDim.x) accept_path[r0 + j] = -1;
+  if (i == 0) {
+    int n = best;
+    for (int j = dbest; j >= 0; --j) {
+      accept_path[r0 + j] = n;
+      n = s_par[n];
+    }
+    accept_len[b] = dbest + 1;
+    bonus[b] = s_amax[best];
+  }
+}
+
+}  // namespace
+
+static void accept_plan(ts_dtype dt, int B, int m, int V, int num_sms, int* S_out, int* seg_out) {
+  if (num_sms < 1) num_sms = 1;
+  const long long rows = static_cast<long long>(B) * m;
+  const int gran = dt == TS_BF16 ? 8 : 4;
+  int S = (V + 65535) / 65536;
+  const long long want = (4LL * num_sms + rows - 1) / rows;
+  if (want > S) S = static_cast<int>(want);
+  const int max_by_len = (V + 2047) / 2048;
+  if (S > max_by_len) S = max_by_len;
+  if (S < 1) S = 1;
+  int seg = (V + S - 1) / S;
+  seg = (seg + gran - 1) / gran * gran;
+  S = (V + seg - 1) / seg;
+  *S_out = S;
+  *seg_out = seg;
+}
+
+size_t tree_accept_workspace_bytes(ts_dtype dt, int B, int m, int V, int num_sms) {
+  int S, seg;
+  accept_plan(dt, B, m, V, num_sms, &S, &seg);
+  return static_cast<size_t>(B) * m * S * 8 + 256;
+}
+
+int tree_accept_launch(const void* logits, ts_dtype dt, const int32_t* tokens,
+                       const int32_t* parents, int B, int m, int V, int32_t* argmax,
+                       int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
+                       int32_t* dev_status, cudaStream_t stream, int num_sms) {
+  int S, seg;
+  accept_plan(dt, B, m, V, num_sms, &S, &seg);
+  const long long rows = static_cast<long long>(B) * m;
+  float* part_v = static_cast<float*>(workspace);
+  int* part_i = reinterpret_cast<int*>(part_v + rows * S);
+  const long long grid = rows * S;
+  if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
+  if (dt == TS_BF16) {
+    const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    argmax_bf16_kernel<<<static_cast<unsigned>(grid), kArgThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(logits), V, seg, S, vec, part_v, part_i);
+  } else {
+    const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    argmax_f32_kernel<<<static_cast<unsigned>(grid), kArgThreads, 0, stream>>>(
+        static_cast<const float*>(logits), V, seg, S, vec, part_v, part_i);
+  }
+  accept_kernel<<<B, kAcceptThreads, 0, stream>>>(part_v, part_i, S, tokens, parents, m, argmax,
+                                                   accept_len, accept_path, bonus, dev_status);
+  count_launches(2);
+  return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+}  // namespace ts

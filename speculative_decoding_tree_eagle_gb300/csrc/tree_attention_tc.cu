@@ -1,0 +1,628 @@
+// ts_tree_attention, tensor-core path (bf16, head dim 128) for sm_103a.
+//
+// Source: "rainlin.net/posts/eagle", section 四 Tree Attention (node i attends to the
+// prefix and to its own root-to-node ancestors only; one pass verifies every path);
+// "lesty.tech — EAGLE-2 vs. Medusa", section 5 (the tree mask stays on chip, no global
+// re-reads) and section 8 (tree K/V sit in the same paged sequence after the prefix).
+//
+// Work unit: (sequence b, KV head, row group, chunk of 64-key tiles).  The g query heads
+// that share a KV head and the m tree nodes are packed into GEMM rows, row = node*g +
+// head-in-group, so every K/V byte fetched from HBM serves m*g query rows on the tensor
+// cores.  A row group is one or two 128-row M tiles (NM).
+//
+// Warp roles (one CTA, 128*(1+NM) + 128 threads):
+//   warp 0      TMA producer: per 64-key tile, one box of min(block_size,64) rows x 64
+//               bf16 (128-byte swizzle) per page and head-dim half for K and for V, from the
+//               block table; positions past the sequence come from an out-of-range block
+//               (zero fill).  STAGES-deep ring, full/empty mbarriers.
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer:
+//                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
+//                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
+//               issued ping-pong over the M tiles so one tile's softmax overlaps the other
+//               tile's MMAs; completion is signalled with tcgen05.commit.
+//   warps 4..   softmax, one thread per row (TMEM lane): load S, apply the tree mask on the
+//               tiles that reach the tree, online softmax in the log2 domain with lazy
+//               rescaling of O (only when the running max grows by more than 2^8), write P
+//               as bf16 into TMEM, then the epilogue (O / l, or an fp32 partial for the
+//               split-K combine).
+// TMEM columns: O_i at 128*i, S_i at 128*NM + 64*i, P_i at 192*NM + 32*i.  P never aliases
+// S, so the next S = Q K^T can run while the previous P V still reads P; a softmax pass
+// starts only after the commit that covers both the new S and the previous P V.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+namespace tc {
+
+constexpr int BN = 64;    // keys per tile
+constexpr int BM = 128;   // rows per M tile
+constexpr int HD = 128;   // head dim
+constexpr uint32_t QHALF = BM * 128;   // 128 rows x 64 bf16 = 16 KB
+constexpr uint32_t QTILE = 2 * QHALF;  // both head-dim halves
+constexpr uint32_t KHALF = BN * 128;   // 64 keys x 64 bf16 = 8 KB
+constexpr uint32_t KTILE = 2 * KHALF;  // 16 KB
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int NM>
+struct Cfg {
+  static constexpr int STAGES = NM == 1 ? 2 : 4;
+  static constexpr int THREADS = 128 + 128 * NM;
+  static constexpr int MIN_BLOCKS = NM == 1 ? 2 : 1;  // two single-tile CTAs share an SM
+  static constexpr uint32_t TMEM_COLS = NM == 1 ? 256 : 512;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = NM * QTILE;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KTILE;
+  static constexpr int NBAR = 4 * STAGES + 3 * NM;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
+};
+
+struct Params {
+  const __nv_bfloat16* q;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const uint64_t* mask;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float2* part_ml;
+  int32_t* status;
+  int m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk;
+  float scale_log2;
+};
+
+// Wait bounded by time only (used on the abort path, to let in-flight copies and MMAs land
+// before shared memory and TMEM are released).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <int NM>
+__global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const Params p) {
+  using C = Cfg<NM>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* sptr = smem_raw + (sbase - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = blockIdx.x, chunk = blockIdx.y, bk = blockIdx.z;
+  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const int L = p.prefix_len[b];
+  if (L < 0 || L > p.max_prefix) {
+    if (threadIdx.x == 0 && rg == 0 && chunk == 0) report(p.status, TS_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int nkeys = L + p.m;
+  const int T = (nkeys + BN - 1) / BN;
+  const int t0 = chunk * p.tpc;
+  if (t0 >= T) return;
+  const int nt = min(p.tpc, T - t0);
+  const int nchunks_b = (T + p.tpc - 1) / p.tpc;
+  const int R0 = rg * NM * BM;
+  const int rows_here = min(p.rows - R0, NM * BM);
+  const int nma = (rows_here + BM - 1) / BM;
+
+  auto bar = [&](int idx) -> uint32_t { return sbase + C::OFF_BAR + 8u * idx; };
+  auto full_k = [&](int s) { return bar(s); };
+  auto full_v = [&](int s) { return bar(ST + s); };
+  auto empty_k = [&](int s) { return bar(2 * ST + s); };
+  auto empty_v = [&](int s) { return bar(3 * ST + s); };
+  auto s_full = [&](int i) { return bar(4 * ST + i); };
+  auto p_full = [&](int i) { return bar(4 * ST + NM + i); };
+  auto o_final = [&](int i) { return bar(4 * ST + 2 * NM + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + C::OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(full_k(s), 1);
+      mbar_init(full_v(s), 1);
+      mbar_init(empty_k(s), 1);
+      mbar_init(empty_v(s), 1);
+    }
+    for (int i = 0; i < NM; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(p_full(i), 128);
+      mbar_init(o_final(i), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  // Q rows of this row group -> shared memory in the 128-byte-swizzled K-major layout
+  // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.
+  for (int c = threadIdx.x; c < NM * BM * 16; c += C::THREADS) {
+    const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
+    const int grow = R0 + row;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (grow < p.rows) {
+      const int node = grow / p.g, head = kvh * p.g + grow % p.g;
+      const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
+      v = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+    }
+    const int i = row >> 7, r = row & 127;
+    *reinterpret_cast<uint4*>(sptr + C::OFF_Q + i * QTILE + h * QHALF + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      const int rpb = min(p.block_size, BN);
+      const int bpt = BN / rpb;
+      int issued = 0;
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % ST;
+        const uint32_t ph = (t / ST) & 1;
+        const int key0 = (t0 + t) * BN;
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
+          const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
+          if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) goto producer_done;
+          mbar_expect_tx(fb, KTILE);
+          const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
+          for (int j = 0; j < bpt; ++j) {
+            const int key = key0 + j * rpb;
+            int blk = p.num_blocks;  // out of range -> the copy fills zeros
+            int rin = 0;
+            if (key < nkeys) {
+              const int e = p.block_table[static_cast<long long>(b) * p.max_blocks + key / p.block_size];
+              if (e >= 0 && e < p.num_blocks) {
+                blk = e;
+                rin = key % p.block_size;
+              } else {
+                report(p.status, TS_ERR_DEVICE_CHECK);
+              }
+            }
+            const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
+            tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
+            tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
+          }
+        }
+        issued = t + 1;
+      }
+    producer_done:
+      if (*abort_flag) {
+        for (int t = max(0, issued - ST); t < issued; ++t) {
+          drain_wait(full_k(t % ST), (t / ST) & 1);
+          drain_wait(full_v(t % ST), (t / ST) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idq = idesc_bf16_f32(128, BN, 0, 0);
+      constexpr uint32_t idp = idesc_bf16_f32(128, HD, 0, 1);
+      auto tS = [&](int i) { return tmem + 128u * NM + 64u * i; };
+      auto tO = [&](int i) { return tmem + 128u * i; };
+      auto tP = [&](int i) { return tmem + 192u * NM + 32u * i; };
+      auto qk = [&](int i, int s) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t h = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + i * QTILE + h * QHALF + ko, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + s * KTILE + h * KHALF + ko, 16, 1024);
+          mma_ss(tS(i), a, bd, idq, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(i));
+      };
+      auto pv = [&](int i, int s, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // B = V tile, MN-major: 64 head-dim columns per 128-byte row, 8-key groups 1 KB
+          // apart (stride offset), the second head-dim half KHALF further (leading offset).
+          const uint64_t bd = sdesc_sw128(sbase + C::OFF_V + s * KTILE + kk * 2048, KHALF, 1024);
+          mma_ts(tO(i), tP(i) + 8u * kk, bd, idp, (first && kk == 0) ? 0u : 1u);
+        }
+      };
+      bool ok = mbar_wait(full_k(0), 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < nma; ++i) qk(i, 0);
+        tc_commit(empty_k(0));
+      }
+      for (int t = 0; ok && t < nt; ++t) {
+        const int s = t % ST;
+        ok = mbar_wait(full_v(s), (t / ST) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        for (int i = 0; i < nma; ++i) {
+          ok = mbar_wait(p_full(i), t & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          pv(i, s, t == 0);
+          if (t + 1 < nt) {
+            const int s1 = (t + 1) % ST;
+            if (i == 0) {
+              ok = mbar_wait(full_k(s1), ((t + 1) / ST) & 1, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            qk(i, s1);
+            if (i == nma - 1) tc_commit(empty_k(s1));
+          }
+        }
+        if (!ok) break;
+        tc_commit(empty_v(s));
+      }
+      for (int i = 0; i < nma; ++i) tc_commit(o_final(i));
+      if (!ok) {
+        for (int i = 0; i < nma; ++i) drain_wait(o_final(i), 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------ softmax + epilogue ------------------------------
+    const int i = (warp - 4) >> 2;
+    const int q4 = warp & 3;
+    if (i < nma) {
+      const int r = q4 * 32 + lane;
+      const int grow = R0 + i * BM + r;
+      const bool valid = grow < p.rows;
+      const int node = valid ? grow / p.g : 0;
+      const int head = kvh * p.g + (valid ? grow % p.g : 0);
+      uint64_t mw0 = 0, mw1 = 0, mw2 = 0, mw3 = 0;
+      if (valid) {
+        const uint64_t* mrow = p.mask + (static_cast<long long>(b) * p.m + node) * p.W;
+        mw0 = mrow[0];
+        if (p.W > 1) mw1 = mrow[1];
+        if (p.W > 2) mw2 = mrow[2];
+        if (p.W > 3) mw3 = mrow[3];
+      }
+      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+      const uint32_t tO = tmem + lane_off + 128u * i;
+      const uint32_t tS = tmem + lane_off + 128u * NM + 64u * i;
+      const uint32_t tP = tmem + lane_off + 192u * NM + 32u * i;
+      const float sl2 = p.scale_log2;
+      float m_ref = -INFINITY, l_sum = 0.f;
+      bool ok = true;
+      for (int t = 0; t < nt; ++t) {
+        ok = mbar_wait_warp(s_full(i), t & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        float s[BN];
+        {
+          uint32_t u[32];
+          tmem_ld32(tS, u);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(u[c]);
+          tmem_ld32(tS + 32, u);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(u[c]);
+        }
+        const int key0 = (t0 + t) * BN;
+        float mx = -INFINITY;
+        if (key0 + BN > L) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int key = key0 + c;
+            bool vis = key < L;
+            if (!vis && key < nkeys) {
+              const int tt = key - L;
+              const uint64_t w = tt < 64 ? mw0 : tt < 128 ? mw1 : tt < 192 ? mw2 : mw3;
+              vis = (w >> (tt & 63)) & 1ull;
+            }
+            s[c] = vis ? s[c] : -INFINITY;
+            mx = fmaxf(mx, s[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        }
+        if (!valid) mx = -INFINITY;
+        const float mt = mx * sl2;
+        float alpha = 1.f;
+        int resc = 0;
+        if (mt > m_ref + kRescaleThreshold) {
+          if (m_ref != -INFINITY) {
+            alpha = ex2_approx(m_ref - mt);
+            resc = 1;
+          }
+          l_sum *= alpha;
+          m_ref = mt;
+        }
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        uint32_t pk[32];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = valid ? ex2_approx(fmaf(s[2 * c], sl2, -mu)) : 0.f;
+          const float p1 = valid ? ex2_approx(fmaf(s[2 * c + 1], sl2, -mu)) : 0.f;
+          rs += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l_sum += rs;
+        tmem_st32(tP, pk);
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * cc, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(tO + 32u * cc, o);
+          }
+        }
+        tmem_st_wait();
+        if (i == 0 && key0 + BN > nkeys) {
+          // zero V rows past the end of the sequence (their P is 0, but the cache slots may
+          // hold non-finite garbage and 0 * inf would poison O)
+          const int s_ = t % ST;
+          ok = mbar_wait_warp(full_v(s_), (t / ST) & 1, abort_flag, p.status);
+          if (!ok) break;
+          const int jv = nkeys - key0;
+          const int nz = (BN - jv) * 16;
+          for (int c = q4 * 32 + lane; c < nz; c += 128) {
+            const int row = jv + (c >> 4), h = (c >> 3) & 1, j = c & 7;
+            *reinterpret_cast<uint4*>(sptr + C::OFF_V + s_ * KTILE + h * KHALF + row * 128 + j * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(p_full(i));
+      }
+      if (ok) ok = mbar_wait_warp(o_final(i), 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        if (nchunks_b == 1) {
+          const float inv = (valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
+          __nv_bfloat16* dst = p.out + ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * cc, o);
+            if (valid) {
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                *reinterpret_cast<uint4*>(dst + cc * 32 + v4 * 8) = w;
+              }
+            }
+          }
+          if (valid && p.lse != nullptr)
+            p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] =
+                (m_ref + log2f(l_sum)) * 0.69314718055994530942f;
+        } else {
+          const long long prow = (static_cast<long long>(bk) * p.rows + grow) * p.nchunk + chunk;
+          float* dst = p.part_o + prow * HD;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * cc, o);
+            if (valid) {
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                *reinterpret_cast<float4*>(dst + cc * 32 + v4 * 4) =
+                    make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
+                                __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+            }
+          }
+          if (valid) p.part_ml[prow] = make_float2(m_ref, l_sum);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Split-K merge: one warp per (sequence, KV head, row); rows of sequences that fit in one
+// chunk were written directly by the attention kernel and are skipped.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
+                                                      const float2* __restrict__ part_ml,
+                                                      const int32_t* __restrict__ prefix_len,
+                                                      Params p, int total_rows) {
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= total_rows) return;
+  const int bk = wid / p.rows, grow = wid % p.rows;
+  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const int L = prefix_len[b];
+  if (L < 0 || L > p.max_prefix) return;
+  const int T = (L + p.m + BN - 1) / BN;
+  const int nch = (T + p.tpc - 1) / p.tpc;
+  if (nch <= 1) return;
+  const long long prow = static_cast<long long>(wid) * p.nchunk;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) {
+    const float2 ml = part_ml[prow + c];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Ls = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float2 ml = part_ml[prow + c];
+    if (!(ml.y > 0.f)) continue;
+    const float w = exp2f(ml.x - M);
+    Ls += w * ml.y;
+    const float4 o = reinterpret_cast<const float4*>(part_o + (prow + c) * HD)[lane];
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  const int node = grow / p.g, head = kvh * p.g + grow % p.g;
+  const long long oo = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + lane * 4;
+  uint2 w;
+  w.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  w.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + oo) = w;
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] =
+        (M + log2f(Ls)) * 0.69314718055994530942f;
+}
+
+struct Plan {
+  int NM, rowgroups, nc, tpc;
+};
+
+static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms) {
+  Plan pl;
+  if (num_sms < 1) num_sms = 1;
+  const int rows = m * (Hq / Hkv);
+  pl.NM = rows > BM ? 2 : 1;
+  pl.rowgroups = (rows + pl.NM * BM - 1) / (pl.NM * BM);
+  const int T = (max_prefix + m + BN - 1) / BN;
+  const long long units = static_cast<long long>(B) * Hkv * pl.rowgroups;
+  const long long slots = static_cast<long long>(num_sms) * (pl.NM == 1 ? 2 : 1);
+  // makespan model in tile units: waves x (tiles per chunk + fixed cost per CTA); a split
+  // adds the partial write + combine read of the CTA's rows (in 64-key-tile equivalents)
+  const int c0 = 3;
+  const int cpart = (pl.NM * BM * 2) / BN;
+  long long best = -1;
+  int best_nc = 1;
+  const int max_nc = T < 512 ? T : 512;
+  for (int nc = 1; nc <= max_nc; ++nc) {
+    const int tpc = (T + nc - 1) / nc;
+    const int ncr = (T + tpc - 1) / tpc;
+    if (ncr != nc) continue;
+    const long long waves = (units * nc + slots - 1) / slots;
+    const long long cost = waves * (tpc + c0 + (nc > 1 ? cpart : 0));
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_nc = nc;
+    }
+  }
+  pl.nc = best_nc;
+  pl.tpc = (T + best_nc - 1) / best_nc;
+  return pl;
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
+
+static bool encode_kv_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int bs) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(bs),
+                              static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(HD) * 2, static_cast<cuuint64_t>(bs) * HD * 2,
+                                 static_cast<cuuint64_t>(Hkv) * bs * HD * 2};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(bs < BN ? bs : BN), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NM>
+static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, const Plan& pl,
+                     int B, int Hkv, cudaStream_t stream) {
+  using C = Cfg<NM>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(tree_attn_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return TS_ERR_CUDA;
+  dim3 grid(pl.rowgroups, pl.nc, B * Hkv);
+  tree_attn_tc_kernel<NM><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, prm);
+  return TS_OK;
+}
+
+}  // namespace tc
+
+bool attention_uses_tc(ts_dtype dt, int d, int block_size) {
+  return dt == TS_BF16 && d == tc::HD &&
+         (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128);
+}
+
+size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms) {
+  const tc::Plan pl = tc::make_plan(B, m, Hq, Hkv, max_prefix, num_sms);
+  if (pl.nc <= 1) return 256;
+  const size_t prow = static_cast<size_t>(B) * Hkv * m * (Hq / Hkv) * pl.nc;
+  return prow * tc::HD * 4 + prow * 8 + 512;
+}
+
+int attention_tc_launch(const AttnArgs& a, int num_sms) {
+  const tc::Plan pl = tc::make_plan(a.B, a.m, a.Hq, a.Hkv, a.max_prefix, num_sms);
+  CUtensorMap mk, mv;
+  if (!tc::encode_kv_map(&mk, a.k_cache, a.num_blocks, a.Hkv, a.block_size) ||
+      !tc::encode_kv_map(&mv, a.v_cache, a.num_blocks, a.Hkv, a.block_size))
+    return TS_ERR_CUDA;
+  tc::Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_table = a.block_table;
+  prm.prefix_len = a.prefix_len;
+  prm.mask = a.mask;
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.lse = a.lse;
+  prm.status = a.dev_status;
+  prm.m = a.m;
+  prm.Hq = a.Hq;
+  prm.Hkv = a.Hkv;
+  prm.g = a.Hq / a.Hkv;
+  prm.rows = a.m * prm.g;
+  prm.W = (a.m + 63) / 64;
+  prm.max_blocks = a.max_blocks;
+  prm.num_blocks = a.num_blocks;
+  prm.block_size = a.block_size;
+  prm.max_prefix = a.max_prefix;
+  prm.tpc = pl.tpc;
+  prm.nchunk = pl.nc;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  const size_t prow = static_cast<size_t>(a.B) * a.Hkv * prm.rows * pl.nc;
+  prm.part_o = pl.nc > 1 ? static_cast<float*>(a.workspace) : nullptr;
+  prm.part_ml = pl.nc > 1 ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * tc::HD * 4)
+                          : nullptr;
+  const int rc = pl.NM == 1 ? tc::launch_nm<1>(mk, mv, prm, pl, a.B, a.Hkv, a.stream)
+                            : tc::launch_nm<2>(mk, mv, prm, pl, a.B, a.Hkv, a.stream);
+  if (rc != TS_OK) return rc;
+  int launches = 1;
+  if (pl.nc > 1) {
+    const int total_rows = a.B * a.Hkv * prm.rows;
+    tc::combine_kernel<<<(total_rows + 7) / 8, 256, 0, a.stream>>>(prm.part_o, prm.part_ml, a.prefix_len,
+                                                                   prm, total_rows);
+    ++launches;
+  }
+  count_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+}  // namespace ts

@@ -1,0 +1,436 @@
+// ts_tree_build kernels: EAGLE-2 dynamic draft-tree construction.
+//
+// Source: "rainlin.net/posts/eagle" (EAGLE series), section 7.1 Expansion and section 7.2
+// Reranking; section 四 for the flattened order and the mask; "lesty.tech — EAGLE-2 vs.
+// Medusa", section 5 for the parent-walk mask.
+//
+// Two launches:
+//   1. row_topk_kernel — the HBM stream.  Every draft row [V] fp32 is split into S
+//      segments; one CTA per (row, segment) keeps a per-thread sorted top-k in registers
+//      while streaming the segment with 16-byte loads, then merges its 256 lists to one
+//      top-k with warp shuffles.  Partials go to the workspace.
+//   2. tree_kernel — one CTA per sequence, all on chip: merge each row's S partial lists,
+//      expand layer by layer (value = parent value + log-prob, fp64, root -> leaf order),
+//      pick each layer's frontier by rank, rerank every candidate with per-layer binary
+//      searches, flatten by (depth, parent position, child rank), and build each node's
+//      ancestor mask by walking its parent pointers.
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+namespace {
+
+constexpr int kTopkThreads = 256;
+constexpr int kTreeThreads = 256;
+
+template <int KM>
+__device__ __forceinline__ void topk_insert(float (&vals)[KM], int (&ids)[KM], float v, int i) {
+  if (!better(v, i, vals[KM - 1], ids[KM - 1])) return;
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    const bool b = better(v, i, vals[j], ids[j]);
+    const float tv = vals[j];
+    const int ti = ids[j];
+    vals[j] = b ? v : tv;
+    ids[j] = b ? i : ti;
+    v = b ? tv : v;
+    i = b ? ti : i;
+  }
+}
+
+template <int KM>
+__device__ __forceinline__ void topk_pop(float (&vals)[KM], int (&ids)[KM]) {
+#pragma unroll
+  for (int j = 0; j < KM - 1; ++j) {
+    vals[j] = vals[j + 1];
+    ids[j] = ids[j + 1];
+  }
+  vals[KM - 1] = -INFINITY;
+  ids[KM - 1] = INT_MAX;
+}
+
+// Best (value, index) across the warp; every lane gets it.
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// Pop the k best of the warp's per-lane sorted lists, in order.  Lane r keeps the r-th.
+template <int KM>
+__device__ __forceinline__ void warp_merge_topk(float (&vals)[KM], int (&ids)[KM], int k,
+                                                float& out_v, int& out_i) {
+  const int lane = threadIdx.x & 31;
+  out_v = -INFINITY;
+  out_i = INT_MAX;
+  for (int r = 0; r < k; ++r) {
+    float hv = vals[0];
+    int hi = ids[0];
+    warp_best(hv, hi);
+    if (ids[0] == hi && vals[0] == hv) topk_pop(vals, ids);
+    if (lane == r) {
+      out_v = hv;
+      out_i = hi;
+    }
+  }
+}
+
+template <int KM>
+__global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
+    const float* __restrict__ logp, int V, int seg_len, int S, int k, int vec,
+    float* __restrict__ part_v, int* __restrict__ part_i) {
+  const long long row = blockIdx.x / S;
+  const int seg = blockIdx.x % S;
+  const float* x = logp + row * static_cast<long long>(V);
+  const int begin = seg * seg_len;
+  const int end = min(V, begin + seg_len);
+  float vals[KM];
+  int ids[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    vals[j] = -INFINITY;
+    ids[j] = INT_MAX;
+  }
+  if (vec) {
+    // 16-byte loads; 4 in flight per thread per iteration.
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int b4 = begin >> 2, e4 = end >> 2;
+    int i = b4 + threadIdx.x;
+    for (; i + 3 * kTopkThreads < e4; i += 4 * kTopkThreads) {
+      float4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = __ldcs(x4 + i + u * kTopkThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int base = (i + u * kTopkThreads) << 2;
+        topk_insert(vals, ids, a[u].x, base);
+        topk_insert(vals, ids, a[u].y, base + 1);
+        topk_insert(vals, ids, a[u].z, base + 2);
+        topk_insert(vals, ids, a[u].w, base + 3);
+      }
+    }
+    for (; i < e4; i += kTopkThreads) {
+      const float4 a = __ldcs(x4 + i);
+      const int base = i << 2;
+      topk_insert(vals, ids, a.x, base);
+      topk_insert(vals, ids, a.y, base + 1);
+      topk_insert(vals, ids, a.z, base + 2);
+      topk_insert(vals, ids, a.w, base + 3);
+    }
+  } else {
+    for (int i = begin + threadIdx.x; i < end; i += kTopkThreads) topk_insert(vals, ids, __ldcs(x + i), i);
+  }
+
+  __shared__ float s_v[kTopkThreads / 32][KM];
+  __shared__ int s_i[kTopkThreads / 32][KM];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float wv;
+  int wi;
+  warp_merge_topk(vals, ids, k, wv, wi);
+  if (lane < k) {
+    s_v[warp][lane] = wv;
+    s_i[warp][lane] = wi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      const bool have = lane < kTopkThreads / 32 && j < k;
+      vals[j] = have ? s_v[lane][j] : -INFINITY;
+      ids[j] = have ? s_i[lane][j] : INT_MAX;
+    }
+    warp_merge_topk(vals, ids, k, wv, wi);
+    if (lane < k) {
+      const long long o = (row * S + seg) * k + lane;
+      part_v[o] = wv;
+      part_i[o] = wi;
+    }
+  }
+}
+
+// Shared-memory layout of tree_kernel (sizes depend on k, depth, R).
+struct TreeSmem {
+  int N;        // candidates
+  int off_rtok, off_rlp, off_val, off_tok, off_lrank, off_sorted, off_flat, off_front, off_sel;
+  int off_cnt, off_par, off_mask, total;
+};
+
+__host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
+
+__host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, int m) {
+  TreeSmem L;
+  L.N = k + (depth - 1) * k * k;
+  int o = 0;
+  L.off_val = o;    o = align8(o + 8 * L.N);            // double V
+  L.off_rtok = o;   o = align8(o + 4 * R * k);          // row top-k tokens
+  L.off_rlp = o;    o = align8(o + 4 * R * k);          // row top-k log-probs
+  L.off_tok = o;    o = align8(o + 4 * L.N);            // candidate token
+  L.off_lrank = o;  o = align8(o + 2 * L.N);            // rank within its layer
+  L.off_sorted = o; o = align8(o + 2 * L.N);            // per layer: ids by rank
+  L.off_flat = o;   o = align8(o + 2 * L.N);            // flat index or -1
+  L.off_front = o;  o = align8(o + 2 * depth * k);      // frontier ids per layer
+  L.off_sel = o;    o = align8(o + L.N);                // selected flag
+  L.off_cnt = o;    o = align8(o + 4 * (depth + 2));    // selected count per layer
+  L.off_par = o;    o = align8(o + 4 * m);              // flat parent
+  L.off_mask = o;   o = align8(o + 4);                  // error flag
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ int layer_base(int l, int k) {  // first candidate id of layer l >= 1
+  return l == 1 ? 0 : k + (l - 2) * k * k;
+}
+__device__ __forceinline__ int layer_size(int l, int k) { return l == 1 ? k : k * k; }
+
+__global__ void __launch_bounds__(kTreeThreads) tree_kernel(
+    const float* __restrict__ part_v, const int* __restrict__ part_i,
+    const int32_t* __restrict__ root_tokens, int R, int S, int k, int depth, int m, int W,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ parents, int32_t* __restrict__ depth_out,
+    uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const TreeSmem L = tree_smem_layout(k, depth, R, m);
+  double* cV = reinterpret_cast<double*>(smem + L.off_val);
+  int* rtok = reinterpret_cast<int*>(smem + L.off_rtok);
+  float* rlp = reinterpret_cast<float*>(smem + L.off_rlp);
+  int* ctok = reinterpret_cast<int*>(smem + L.off_tok);
+  short* lrank = reinterpret_cast<short*>(smem + L.off_lrank);
+  short* sorted = reinterpret_cast<short*>(smem + L.off_sorted);
+  short* cflat = reinterpret_cast<short*>(smem + L.off_flat);
+  short* front = reinterpret_cast<short*>(smem + L.off_front);
+  unsigned char* sel = smem + L.off_sel;
+  int* cnt = reinterpret_cast<int*>(smem + L.off_cnt);
+  int* fpar = reinterpret_cast<int*>(smem + L.off_par);
+  int* err = reinterpret_cast<int*>(smem + L.off_mask);
+
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = kTreeThreads / 32;
+  const long long out0 = static_cast<long long>(b) * m;
+
+  if (tid == 0) *err = 0;
+  if (m > 1) {
+    // 1. Merge each row's S sorted segment lists (k each) into the row's top-k.
+    for (int r = warp; r < R; r += nwarps) {
+      const long long base = (static_cast<long long>(b) * R + r) * S * k;
+      int ptr = 0;
+      for (int j = 0; j < k; ++j) {
+        float v = -INFINITY;
+        int i = INT_MAX;
+        if (lane < S && ptr < k) {
+          v = part_v[base + lane * k + ptr];
+          i = part_i[base + lane * k + ptr];
+        }
+        float bv = v;
+        int bi = i;
+        warp_best(bv, bi);
+        if (lane < S && ptr < k && i == bi && v == bv) ++ptr;
+        if (lane == 0) {
+          rtok[r * k + j] = bi;
+          rlp[r * k + j] = bv;
+        }
+      }
+    }
+    for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
+    __syncthreads();
+
+    // 2. Expansion, layer by layer.
+    for (int l = 1; l <= depth; ++l) {
+      const int base = layer_base(l, k), n = layer_size(l, k);
+      for (int t = tid; t < n; t += kTreeThreads) {
+        if (l == 1) {
+          ctok[t] = rtok[t];
+          cV[t] = 0.0 + static_cast<double>(rlp[t]);
+        } else {
+          const int j = t / k, c = t % k;
+          const int par = front[(l - 2) * k + j];
+          const int row = 1 + (l - 2) * k + j;
+          ctok[base + t] = rtok[row * k + c];
+          cV[base + t] = cV[par] + static_cast<double>(rlp[row * k + c]);
+        }
+      }
+      __syncthreads();
+      // rank inside the layer: value descending, ties -> lower layer-local index
+      for (int t = tid; t < n; t += kTreeThreads) {
+        const double v = cV[base + t];
+        int rank = 0;
+        for (int y = 0; y < n; ++y) {
+          const double w = cV[base + y];
+          rank += (w > v || (w == v && y < t)) ? 1 : 0;
+        }
+        lrank[base + t] = static_cast<short>(rank);
+        sorted[base + rank] = static_cast<short>(base + t);
+      }
+      __syncthreads();
+      if (tid < k) front[(l - 1) * k + tid] = sorted[base + tid];
+      __syncthreads();
+    }
+
+    // 3. Rerank: global rank = rank in own layer + per-other-layer counts of better
+    //    candidates (value higher, or equal and shallower), by binary search.
+    for (int x = tid; x < L.N; x += kTreeThreads) {
+      int l = 1;
+      while (l < depth && x >= layer_base(l + 1, k)) ++l;
+      const double v = cV[x];
+      int g = lrank[x];
+      for (int l2 = 1; l2 <= depth; ++l2) {
+        if (l2 == l) continue;
+        const int base2 = layer_base(l2, k), n2 = layer_size(l2, k);
+        const bool shallower = l2 < l;
+        int lo = 0, hi = n2;  // count of the sorted prefix that beats x
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          const double w = cV[sorted[base2 + mid]];
+          const bool beats = shallower ? (w >= v) : (w > v);
+          if (beats) lo = mid + 1; else hi = mid;
+        }
+        g += lo;
+      }
+      const bool s = g < m - 1;
+      sel[x] = s ? 1 : 0;
+      cflat[x] = -1;
+      if (s) atomicAdd(&cnt[l], 1);
+    }
+    __syncthreads();
+    // connectivity: every selected node's parent must be selected
+    for (int x = tid; x < L.N; x += kTreeThreads) {
+      if (!sel[x] || x < k) continue;
+      int l = 2;
+      while (l < depth && x >= layer_base(l + 1, k)) ++l;
+      const int j = (x - layer_base(l, k)) / k;
+      if (!sel[front[(l - 2) * k + j]]) *err = 1;
+    }
+    __syncthreads();
+    if (*err) {
+      if (tid == 0) report(status, TS_ERR_DEVICE_CHECK);
+      return;
+    }
+
+    // 4. Flatten: root, then by (depth, parent's flat index, child rank).
+    int off = 1;
+    for (int l = 1; l <= depth; ++l) {
+      const int base = layer_base(l, k), n = layer_size(l, k);
+      for (int t = tid; t < n; t += kTreeThreads) {
+        const int x = base + t;
+        if (!sel[x]) continue;
+        const int c = t % k;
+        const int pf = (l == 1) ? 0 : cflat[front[(l - 2) * k + t / k]];
+        int pos = 0;
+        for (int u = 0; u < n; ++u) {
+          const int y = base + u;
+          if (!sel[y] || y == x) continue;
+          const int pfy = (l == 1) ? 0 : cflat[front[(l - 2) * k + u / k]];
+          const int cy = u % k;
+          pos += (pfy < pf || (pfy == pf && cy < c)) ? 1 : 0;
+        }
+        const int f = off + pos;
+        cflat[x] = static_cast<short>(f);
+        fpar[f] = pf;
+        tokens[out0 + f] = ctok[x];
+        parents[out0 + f] = pf;
+        depth_out[out0 + f] = l;
+        if (values) values[out0 + f] = cV[x];
+      }
+      off += cnt[l];
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    fpar[0] = -1;
+    tokens[out0] = root_tokens[b];
+    parents[out0] = -1;
+    depth_out[out0] = 0;
+    if (values) values[out0] = 0.0;
+  }
+  __syncthreads();
+  // 5. Mask rows: walk the parent pointers from each node to the root.
+  for (int i = tid; i < m; i += kTreeThreads) {
+    uint64_t w[TS_MAX_NODES / 64] = {0, 0, 0, 0};
+    int n = i;
+    for (int steps = 0; n >= 0 && steps <= m; ++steps) {
+      w[n >> 6] |= 1ull << (n & 63);
+      n = fpar[n];
+    }
+    for (int q = 0; q < W; ++q) mask[(out0 + i) * W + q] = w[q];
+  }
+}
+
+}  // namespace
+
+// Segments per draft row: enough CTAs to cover the GPU, at most 32 (one per lane of the
+// merge warp), segment length a multiple of 4 (16-byte loads), at least 2048 floats.
+static void build_plan(int B, int V, int k, int depth, int num_sms, int* S_out, int* seg_out) {
+  if (num_sms < 1) num_sms = 1;
+  const int R = 1 + (depth - 1) * k;
+  const long long rows = static_cast<long long>(B) * R;
+  int S = (V + 16383) / 16384;
+  const long long want = (2LL * num_sms + rows - 1) / rows;
+  if (want > S) S = static_cast<int>(want);
+  const int max_by_len = (V + 2047) / 2048;
+  if (S > max_by_len) S = max_by_len;
+  if (S > 32) S = 32;
+  if (S < 1) S = 1;
+  int seg = (V + S - 1) / S;
+  seg = (seg + 3) & ~3;
+  S = (V + seg - 1) / seg;
+  *S_out = S;
+  *seg_out = seg;
+}
+
+size_t tree_build_workspace_bytes(int B, int V, int k, int depth, int num_sms) {
+  int S, seg;
+  build_plan(B, V, k, depth, num_sms, &S, &seg);
+  const long long R = 1 + static_cast<long long>(depth - 1) * k;
+  return static_cast<size_t>(B) * R * S * k * 8 + 256;
+}
+
+int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
+                      int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
+                      uint64_t* mask, double* values, void* workspace, int32_t* dev_status,
+                      cudaStream_t stream, int num_sms) {
+  const int R = 1 + (depth - 1) * k;
+  int S, seg;
+  build_plan(B, V, k, depth, num_sms, &S, &seg);
+  const long long rows = static_cast<long long>(B) * R;
+  float* part_v = static_cast<float*>(workspace);
+  int* part_i = reinterpret_cast<int*>(part_v + rows * S * k);
+  const int W = (m + 63) / 64;
+  int launches = 0;
+  if (m > 1) {
+    const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(draft_logp) % 16 == 0);
+    const long long grid = rows * S;
+    if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
+#define TS_TOPK(KM)                                                                     \
+  row_topk_kernel<KM><<<static_cast<unsigned>(grid), kTopkThreads, 0, stream>>>(        \
+      draft_logp, V, seg, S, k, vec, part_v, part_i)
+    if (k <= 2) TS_TOPK(2);
+    else if (k <= 4) TS_TOPK(4);
+    else if (k <= 8) TS_TOPK(8);
+    else TS_TOPK(16);
+#undef TS_TOPK
+    ++launches;
+  }
+  const TreeSmem L = tree_smem_layout(k, depth, R, m);
+  const int smem = L.total;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return TS_ERR_CUDA;
+  }
+  tree_kernel<<<B, kTreeThreads, smem, stream>>>(part_v, part_i, root_tokens, R, S, k, depth, m,
+                                                  W, tokens, parents, depth_out, mask, values,
+                                                  dev_status);
+  ++launches;
+  count_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+}
+
+}  // namespace ts

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host-side
+validation rejects bad arguments before any launch (CPU only: no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_tree_eagle_gb300 as ts
+from speculative_decoding_tree_eagle_gb300 import build as tsbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treespec.h")
+
+TS_OK, TS_ERR_INVALID, TS_ERR_UNSUPPORTED = 0, -1, -2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tsbuild.build()
+    return ts.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ts_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    syms = declared_symbols()
+    for s in ("ts_tree_build", "ts_tree_attention", "ts_tree_accept"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+
+
+def test_status_strings(lib):
+    assert ts.status_string(0) == "TS_OK"
+    for c in (-1, -2, -3, -4, -5, -6):
+        assert ts.status_string(c).startswith("TS_ERR_")
+    assert lib.ts_version() == 1
+
+
+def _build(lib, B=1, V=100, k=2, depth=3, m=8, ptr=1):
+    P = ptr
+    return lib.ts_tree_build(P, P, B, V, k, depth, m, P, P, P, P, None, P, 1 << 20, None, None)
+
+
+def test_tree_build_validation(lib):
+    assert _build(lib, B=0) == TS_ERR_INVALID
+    assert _build(lib, m=0) == TS_ERR_INVALID
+    assert _build(lib, k=17) == TS_ERR_UNSUPPORTED
+    assert _build(lib, depth=17) == TS_ERR_UNSUPPORTED
+    assert _build(lib, m=257) == TS_ERR_UNSUPPORTED
+    assert _build(lib, m=12) == TS_ERR_INVALID          # m-1 > k + (depth-1)k^2 = 10
+    assert _build(lib, V=1) == TS_ERR_INVALID           # k > V
+    assert _build(lib, ptr=None) == TS_ERR_INVALID      # null pointers
+    assert lib.ts_tree_build_workspace(1, 100, 2, 3, 12) == 0
+
+
+def _attn(lib, dt=1, B=1, m=8, Hq=4, Hkv=1, d=128, maxp=64, nb=10, bs=16, mb=8, scale=0.1, ptr=1):
+    P = ptr
+    return lib.ts_tree_attention(P, P, P, dt, nb, bs, P, mb, P, maxp, P, B, m, Hq, Hkv, d, scale, P, None,
+                                 P, 1 << 20, None, None)
+
+
+def test_tree_attention_validation(lib):
+    assert _attn(lib, Hq=6, Hkv=4) == TS_ERR_INVALID          # Hq % Hkv
+    assert _attn(lib, dt=7) == TS_ERR_INVALID
+    assert _attn(lib, m=300) == TS_ERR_UNSUPPORTED
+    assert _attn(lib, d=512) == TS_ERR_UNSUPPORTED
+    assert _attn(lib, maxp=-1) == TS_ERR_INVALID
+    assert _attn(lib, mb=4) == TS_ERR_INVALID                 # 4*16 < 64 + 8
+    assert _attn(lib, ptr=None) == TS_ERR_INVALID
+    assert _attn(lib, scale=float("nan")) == TS_ERR_INVALID
+    assert _attn(lib, nb=0) == TS_ERR_INVALID
+
+
+def _accept(lib, dt=1, B=1, m=8, V=100, ptr=1):
+    P = ptr
+    return lib.ts_tree_accept(P, dt, P, P, B, m, V, P, P, P, P, P, 1 << 20, None, None)
+
+
+def test_tree_accept_validation(lib):
+    assert _accept(lib, B=0) == TS_ERR_INVALID
+    assert _accept(lib, V=0) == TS_ERR_INVALID
+    assert _accept(lib, dt=3) == TS_ERR_INVALID
+    assert _accept(lib, m=257) == TS_ERR_UNSUPPORTED
+    assert _accept(lib, ptr=None) == TS_ERR_INVALID
+
+
+def test_workspace_queries_are_positive_for_valid_sizes(lib):
+    assert lib.ts_tree_build_workspace(8, 128256, 10, 7, 64) > 0
+    assert lib.ts_tree_accept_workspace(1, 8, 64, 128256) > 0
+    assert lib.ts_tree_attention_workspace(1, 4, 128, 32, 8, 128, 32768) > 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        ts.tree_accept(torch.zeros(1, 2, 4), torch.zeros(1, 2, dtype=torch.int32),
+                       torch.zeros(1, 2, dtype=torch.int32))
