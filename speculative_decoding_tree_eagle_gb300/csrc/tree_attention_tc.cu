@@ -550,6 +550,39 @@ static bool encode_kv_map(CUtensorMap* map, const void* base, int num_blocks, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Small cache of encoded K/V tensor maps keyed by (base pointer, shape): encoding is a
+// host-side driver call, and serving loops reuse the same cache tensors every step.
+struct MapEntry {
+  const void* base;
+  int num_blocks, Hkv, bs;
+  CUtensorMap map;
+  uint64_t stamp;
+};
+
+static bool cached_kv_map(CUtensorMap* out, const void* base, int num_blocks, int Hkv, int bs) {
+  constexpr int kSlots = 16;
+  static MapEntry cache[kSlots] = {};
+  static uint64_t clock = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  ++clock;
+  int victim = 0;
+  for (int i = 0; i < kSlots; ++i) {
+    MapEntry& e = cache[i];
+    if (e.stamp != 0 && e.base == base && e.num_blocks == num_blocks && e.Hkv == Hkv && e.bs == bs) {
+      e.stamp = clock;
+      *out = e.map;
+      return true;
+    }
+    if (e.stamp < cache[victim].stamp) victim = i;
+  }
+  MapEntry e{base, num_blocks, Hkv, bs, {}, clock};
+  if (!encode_kv_map(&e.map, base, num_blocks, Hkv, bs)) return false;
+  cache[victim] = e;
+  *out = e.map;
+  return true;
+}
+
 template <int NM>
 static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, const Plan& pl,
                      int B, int Hkv, cudaStream_t stream) {
@@ -583,8 +616,8 @@ size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefi
 int attention_tc_launch(const AttnArgs& a, int num_sms) {
   const tc::Plan pl = tc::make_plan(a.B, a.m, a.Hq, a.Hkv, a.max_prefix, num_sms);
   CUtensorMap mk, mv;
-  if (!tc::encode_kv_map(&mk, a.k_cache, a.num_blocks, a.Hkv, a.block_size) ||
-      !tc::encode_kv_map(&mv, a.v_cache, a.num_blocks, a.Hkv, a.block_size))
+  if (!tc::cached_kv_map(&mk, a.k_cache, a.num_blocks, a.Hkv, a.block_size) ||
+      !tc::cached_kv_map(&mv, a.v_cache, a.num_blocks, a.Hkv, a.block_size))
     return TS_ERR_CUDA;
   tc::Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -24,7 +24,7 @@ namespace ts {
 namespace {
 
 constexpr int kTopkThreads = 256;
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 512;
 
 template <int KM>
 __device__ __forceinline__ void topk_insert(float (&vals)[KM], int (&ids)[KM], float v, int i) {
@@ -157,11 +157,11 @@ __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
   }
 }
 
-// Shared-memory layout of tree_kernel (sizes depend on k, depth, R).
+// Shared-memory layout of tree_kernel (sizes depend on k, depth, R, m).
 struct TreeSmem {
-  int N;        // candidates
-  int off_rtok, off_rlp, off_val, off_tok, off_lrank, off_sorted, off_flat, off_front, off_sel;
-  int off_cnt, off_par, off_mask, total;
+  int N;  // candidates
+  int off_val, off_key, off_rtok, off_rlp, off_tok, off_lrank, off_sorted, off_flat, off_sel;
+  int off_cntc, off_cnt, off_par, off_err, total;
 };
 
 __host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
@@ -170,18 +170,19 @@ __host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, in
   TreeSmem L;
   L.N = k + (depth - 1) * k * k;
   int o = 0;
-  L.off_val = o;    o = align8(o + 8 * L.N);            // double V
-  L.off_rtok = o;   o = align8(o + 4 * R * k);          // row top-k tokens
-  L.off_rlp = o;    o = align8(o + 4 * R * k);          // row top-k log-probs
-  L.off_tok = o;    o = align8(o + 4 * L.N);            // candidate token
-  L.off_lrank = o;  o = align8(o + 2 * L.N);            // rank within its layer
-  L.off_sorted = o; o = align8(o + 2 * L.N);            // per layer: ids by rank
-  L.off_flat = o;   o = align8(o + 2 * L.N);            // flat index or -1
-  L.off_front = o;  o = align8(o + 2 * depth * k);      // frontier ids per layer
-  L.off_sel = o;    o = align8(o + L.N);                // selected flag
-  L.off_cnt = o;    o = align8(o + 4 * (depth + 2));    // selected count per layer
-  L.off_par = o;    o = align8(o + 4 * m);              // flat parent
-  L.off_mask = o;   o = align8(o + 4);                  // error flag
+  L.off_val = o;    o = align8(o + 8 * L.N);              // fp64 value (sum of log-probs)
+  L.off_key = o;    o = align8(o + 8 * L.N);              // order-preserving integer key
+  L.off_rtok = o;   o = align8(o + 4 * R * k);            // row top-k tokens
+  L.off_rlp = o;    o = align8(o + 4 * R * k);            // row top-k log-probs
+  L.off_tok = o;    o = align8(o + 4 * L.N);              // candidate token
+  L.off_lrank = o;  o = align8(o + 2 * L.N);              // rank within its layer
+  L.off_sorted = o; o = align8(o + 2 * L.N);              // per layer: ids by rank
+  L.off_flat = o;   o = align8(o + 2 * L.N);              // flat index or -1
+  L.off_sel = o;    o = align8(o + L.N);                  // selected flag
+  L.off_cntc = o;   o = align8(o + 4 * (depth + 1) * k);  // selected children per frontier slot
+  L.off_cnt = o;    o = align8(o + 4 * (depth + 2));      // selected per layer
+  L.off_par = o;    o = align8(o + 4 * m);                // flat parent
+  L.off_err = o;    o = align8(o + 4);
   L.total = o;
   return L;
 }
@@ -190,6 +191,19 @@ __device__ __forceinline__ int layer_base(int l, int k) {  // first candidate id
   return l == 1 ? 0 : k + (l - 2) * k * k;
 }
 __device__ __forceinline__ int layer_size(int l, int k) { return l == 1 ? k : k * k; }
+__device__ __forceinline__ int layer_of(int x, int k, int depth) {
+  if (x < k) return 1;
+  const int l = 2 + (x - k) / (k * k);
+  return l > depth ? depth : l;
+}
+
+// Monotone map of a double to an unsigned key (larger value -> larger key).  -0 and +0 get
+// the same key, so integer comparisons order values exactly as fp64 comparisons do.
+__device__ __forceinline__ unsigned long long order_key(double v) {
+  if (v == 0.0) v = 0.0;
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
 
 __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     const float* __restrict__ part_v, const int* __restrict__ part_i,
@@ -199,21 +213,22 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
   extern __shared__ __align__(16) unsigned char smem[];
   const TreeSmem L = tree_smem_layout(k, depth, R, m);
   double* cV = reinterpret_cast<double*>(smem + L.off_val);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(smem + L.off_key);
   int* rtok = reinterpret_cast<int*>(smem + L.off_rtok);
   float* rlp = reinterpret_cast<float*>(smem + L.off_rlp);
   int* ctok = reinterpret_cast<int*>(smem + L.off_tok);
   short* lrank = reinterpret_cast<short*>(smem + L.off_lrank);
   short* sorted = reinterpret_cast<short*>(smem + L.off_sorted);
   short* cflat = reinterpret_cast<short*>(smem + L.off_flat);
-  short* front = reinterpret_cast<short*>(smem + L.off_front);
   unsigned char* sel = smem + L.off_sel;
+  int* cntc = reinterpret_cast<int*>(smem + L.off_cntc);
   int* cnt = reinterpret_cast<int*>(smem + L.off_cnt);
   int* fpar = reinterpret_cast<int*>(smem + L.off_par);
-  int* err = reinterpret_cast<int*>(smem + L.off_mask);
+  int* err = reinterpret_cast<int*>(smem + L.off_err);
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = kTreeThreads / 32;
+  constexpr int nwarps = kTreeThreads / 32;
   const long long out0 = static_cast<long long>(b) * m;
 
   if (tid == 0) *err = 0;
@@ -239,74 +254,81 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         }
       }
     }
+    for (int x = tid; x < (depth + 1) * k; x += kTreeThreads) cntc[x] = 0;
     for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
     __syncthreads();
 
-    // 2. Expansion, layer by layer.
+    // 2. Expansion, layer by layer: value = parent value + log-prob (fp64, root -> leaf);
+    //    frontier slot j of layer l-1 is the candidate of rank j in that layer.
     for (int l = 1; l <= depth; ++l) {
       const int base = layer_base(l, k), n = layer_size(l, k);
       for (int t = tid; t < n; t += kTreeThreads) {
+        double v;
+        int tok;
         if (l == 1) {
-          ctok[t] = rtok[t];
-          cV[t] = 0.0 + static_cast<double>(rlp[t]);
+          tok = rtok[t];
+          v = 0.0 + static_cast<double>(rlp[t]);
         } else {
           const int j = t / k, c = t % k;
-          const int par = front[(l - 2) * k + j];
+          const int par = sorted[layer_base(l - 1, k) + j];
           const int row = 1 + (l - 2) * k + j;
-          ctok[base + t] = rtok[row * k + c];
-          cV[base + t] = cV[par] + static_cast<double>(rlp[row * k + c]);
+          tok = rtok[row * k + c];
+          v = cV[par] + static_cast<double>(rlp[row * k + c]);
         }
+        ctok[base + t] = tok;
+        cV[base + t] = v;
+        ckey[base + t] = order_key(v);
       }
       __syncthreads();
       // rank inside the layer: value descending, ties -> lower layer-local index
       for (int t = tid; t < n; t += kTreeThreads) {
-        const double v = cV[base + t];
+        const unsigned long long kv = ckey[base + t];
         int rank = 0;
         for (int y = 0; y < n; ++y) {
-          const double w = cV[base + y];
-          rank += (w > v || (w == v && y < t)) ? 1 : 0;
+          const unsigned long long ky = ckey[base + y];
+          rank += (ky > kv || (ky == kv && y < t)) ? 1 : 0;
         }
         lrank[base + t] = static_cast<short>(rank);
         sorted[base + rank] = static_cast<short>(base + t);
       }
       __syncthreads();
-      if (tid < k) front[(l - 1) * k + tid] = sorted[base + tid];
-      __syncthreads();
     }
 
-    // 3. Rerank: global rank = rank in own layer + per-other-layer counts of better
-    //    candidates (value higher, or equal and shallower), by binary search.
+    // 3. Rerank: global rank = rank in own layer + for every other layer the number of
+    //    its candidates that come first (higher value, or equal value and shallower),
+    //    found by binary search in that layer's sorted order.
     for (int x = tid; x < L.N; x += kTreeThreads) {
-      int l = 1;
-      while (l < depth && x >= layer_base(l + 1, k)) ++l;
-      const double v = cV[x];
+      const int l = layer_of(x, k, depth);
+      const unsigned long long kv = ckey[x];
       int g = lrank[x];
       for (int l2 = 1; l2 <= depth; ++l2) {
         if (l2 == l) continue;
         const int base2 = layer_base(l2, k), n2 = layer_size(l2, k);
         const bool shallower = l2 < l;
-        int lo = 0, hi = n2;  // count of the sorted prefix that beats x
+        int lo = 0, hi = n2;
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
-          const double w = cV[sorted[base2 + mid]];
-          const bool beats = shallower ? (w >= v) : (w > v);
-          if (beats) lo = mid + 1; else hi = mid;
+          const unsigned long long kw = ckey[sorted[base2 + mid]];
+          if (shallower ? (kw >= kv) : (kw > kv)) lo = mid + 1; else hi = mid;
         }
         g += lo;
       }
       const bool s = g < m - 1;
       sel[x] = s ? 1 : 0;
       cflat[x] = -1;
-      if (s) atomicAdd(&cnt[l], 1);
+      if (s) {
+        atomicAdd(&cnt[l], 1);
+        const int slot = (l == 1) ? 0 : (x - layer_base(l, k)) / k;
+        atomicAdd(&cntc[l * k + slot], 1);
+      }
     }
     __syncthreads();
     // connectivity: every selected node's parent must be selected
     for (int x = tid; x < L.N; x += kTreeThreads) {
       if (!sel[x] || x < k) continue;
-      int l = 2;
-      while (l < depth && x >= layer_base(l + 1, k)) ++l;
+      const int l = layer_of(x, k, depth);
       const int j = (x - layer_base(l, k)) / k;
-      if (!sel[front[(l - 2) * k + j]]) *err = 1;
+      if (!sel[sorted[layer_base(l - 1, k) + j]]) *err = 1;
     }
     __syncthreads();
     if (*err) {
@@ -314,23 +336,26 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       return;
     }
 
-    // 4. Flatten: root, then by (depth, parent's flat index, child rank).
+    // 4. Flatten: root, then by (depth, parent's flat index, child rank).  A node's
+    //    position in its depth = selected children of parents placed before its parent
+    //    + selected siblings of lower rank.
     int off = 1;
     for (int l = 1; l <= depth; ++l) {
       const int base = layer_base(l, k), n = layer_size(l, k);
       for (int t = tid; t < n; t += kTreeThreads) {
         const int x = base + t;
         if (!sel[x]) continue;
-        const int c = t % k;
-        const int pf = (l == 1) ? 0 : cflat[front[(l - 2) * k + t / k]];
-        int pos = 0;
-        for (int u = 0; u < n; ++u) {
-          const int y = base + u;
-          if (!sel[y] || y == x) continue;
-          const int pfy = (l == 1) ? 0 : cflat[front[(l - 2) * k + u / k]];
-          const int cy = u % k;
-          pos += (pfy < pf || (pfy == pf && cy < c)) ? 1 : 0;
+        const int j = (l == 1) ? 0 : t / k, c = t % k;
+        int pos = 0, pf = 0;
+        if (l > 1) {
+          const int pbase = layer_base(l - 1, k);
+          pf = cflat[sorted[pbase + j]];
+          for (int j2 = 0; j2 < k; ++j2) {
+            if (j2 == j || cntc[l * k + j2] == 0) continue;
+            if (cflat[sorted[pbase + j2]] < pf) pos += cntc[l * k + j2];
+          }
         }
+        for (int c2 = 0; c2 < c; ++c2) pos += sel[base + j * k + c2];
         const int f = off + pos;
         cflat[x] = static_cast<short>(f);
         fpar[f] = pf;
@@ -353,13 +378,22 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
   __syncthreads();
   // 5. Mask rows: walk the parent pointers from each node to the root.
   for (int i = tid; i < m; i += kTreeThreads) {
-    uint64_t w[TS_MAX_NODES / 64] = {0, 0, 0, 0};
+    uint64_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
     int n = i;
     for (int steps = 0; n >= 0 && steps <= m; ++steps) {
-      w[n >> 6] |= 1ull << (n & 63);
+      const uint64_t bit = 1ull << (n & 63);
+      const int q = n >> 6;
+      w0 |= q == 0 ? bit : 0ull;
+      w1 |= q == 1 ? bit : 0ull;
+      w2 |= q == 2 ? bit : 0ull;
+      w3 |= q == 3 ? bit : 0ull;
       n = fpar[n];
     }
-    for (int q = 0; q < W; ++q) mask[(out0 + i) * W + q] = w[q];
+    uint64_t* dst = mask + (out0 + i) * W;
+    dst[0] = w0;
+    if (W > 1) dst[1] = w1;
+    if (W > 2) dst[2] = w2;
+    if (W > 3) dst[3] = w3;
   }
 }
 

@@ -148,7 +148,8 @@ def generate(w: Workload, with_attention: bool = True, with_logits: bool = True)
     nblk = [math.ceil((int(prefix[b]) + w.m) / BLOCK_SIZE) for b in range(w.B)]
     num_blocks = sum(nblk)
     perm = torch.randperm(num_blocks, generator=gen) if w.shuffled else torch.arange(num_blocks)
-    max_blocks = max(nblk)
+    # table width covers the largest prefix the workload allows (the kernels' host-side bound)
+    max_blocks = max(max(nblk), math.ceil((hi + w.m) / BLOCK_SIZE))
     table = torch.full((w.B, max_blocks), -1, dtype=torch.int32)
     off = 0
     for b in range(w.B):
