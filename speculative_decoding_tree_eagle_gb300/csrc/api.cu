@@ -94,7 +94,6 @@ int ts_tree_build(const float* draft_logp, const int32_t* root_tokens, int B, in
 size_t ts_tree_attention_workspace(ts_dtype dt, int B, int m, int Hq, int Hkv, int d,
                                    int max_prefix) {
   if (ts::check_attention(dt, B, m, Hq, Hkv, d, max_prefix) != TS_OK) return 0;
-  // the tensor-core path with the common 16-row pages; other page sizes plan the same
   if (ts::attention_uses_tc(dt, d, 16))
     return ts::attention_tc_workspace_bytes(B, m, Hq, Hkv, max_prefix, ts::device_sm_count());
   return 256;

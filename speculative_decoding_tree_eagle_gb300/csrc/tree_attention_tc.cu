@@ -48,6 +48,7 @@ constexpr uint32_t QTILE = 2 * QHALF;  // both head-dim halves
 constexpr uint32_t KHALF = BN * 128;   // 64 keys x 64 bf16 = 8 KB
 constexpr uint32_t KTILE = 2 * KHALF;  // 16 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxChunkBoxes = 2048;       // physical-block ids a CTA stages in shared memory
 
 template <int NM>
 struct Cfg {
@@ -61,7 +62,8 @@ struct Cfg {
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KTILE;
   static constexpr int NBAR = 4 * STAGES + 3 * NM;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
+  static constexpr uint32_t OFF_BLK = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_BYTES = OFF_BLK + 4 * kMaxChunkBoxes + 1024;  // + 1 KB alignment slack
 };
 
 struct Params {
@@ -148,17 +150,61 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   }
   // Q rows of this row group -> shared memory in the 128-byte-swizzled K-major layout
   // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.
-  for (int c = threadIdx.x; c < NM * BM * 16; c += C::THREADS) {
-    const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
-    const int grow = R0 + row;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (grow < p.rows) {
-      const int node = grow / p.g, head = kvh * p.g + grow % p.g;
-      const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
-      v = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+  // (loads are issued in batches of 4 per thread so their latencies overlap)
+  for (int c0 = threadIdx.x; c0 < NM * BM * 16; c0 += 4 * C::THREADS) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * C::THREADS;
+      const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
+      const int grow = R0 + row;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < NM * BM * 16 && grow < p.rows) {
+        const int node = grow / p.g, head = kvh * p.g + grow % p.g;
+        const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
+        v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+      }
     }
-    const int i = row >> 7, r = row & 127;
-    *reinterpret_cast<uint4*>(sptr + C::OFF_Q + i * QTILE + h * QHALF + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * C::THREADS;
+      if (c >= NM * BM * 16) break;
+      const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
+      const int i = row >> 7, r = row & 127;
+      *reinterpret_cast<uint4*>(sptr + C::OFF_Q + i * QTILE + h * QHALF + r * 128 + ((j ^ (r & 7)) << 4)) = v[u];
+    }
+  }
+  // Physical block of every TMA box of this chunk -> shared memory (warp 0, coalesced,
+  // 4 independent loads in flight per lane); out-of-range ids are reported and replaced by
+  // the out-of-bounds block, positions past the sequence get the out-of-bounds block too.
+  const int rpb = min(p.block_size, BN);
+  const int bpt = BN / rpb;
+  int* s_blk = reinterpret_cast<int*>(sptr + C::OFF_BLK);
+  if (warp == 0) {
+    const int nbox = nt * bpt;
+    for (int e0 = lane; e0 < nbox; e0 += 4 * 32) {
+      int ids[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + 32 * u;
+        const int key = t0 * BN + e * rpb;
+        ids[u] = -1;
+        if (e < nbox && key < nkeys)
+          ids[u] = __ldg(p.block_table + static_cast<long long>(b) * p.max_blocks + key / p.block_size);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + 32 * u;
+        if (e >= nbox) break;
+        const int key = t0 * BN + e * rpb;
+        int phys = p.num_blocks;
+        if (key < nkeys) {
+          if (ids[u] >= 0 && ids[u] < p.num_blocks) phys = ids[u];
+          else report(p.status, TS_ERR_DEVICE_CHECK);
+        }
+        s_blk[e] = phys;
+      }
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -169,8 +215,6 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      const int rpb = min(p.block_size, BN);
-      const int bpt = BN / rpb;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % ST;
@@ -183,18 +227,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
           mbar_expect_tx(fb, KTILE);
           const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
           for (int j = 0; j < bpt; ++j) {
-            const int key = key0 + j * rpb;
-            int blk = p.num_blocks;  // out of range -> the copy fills zeros
-            int rin = 0;
-            if (key < nkeys) {
-              const int e = p.block_table[static_cast<long long>(b) * p.max_blocks + key / p.block_size];
-              if (e >= 0 && e < p.num_blocks) {
-                blk = e;
-                rin = key % p.block_size;
-              } else {
-                report(p.status, TS_ERR_DEVICE_CHECK);
-              }
-            }
+            const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
+            const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
             const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
             tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
             tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
@@ -455,12 +489,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (nch <= 1) return;
   const long long prow = static_cast<long long>(wid) * p.nchunk;
   float M = -INFINITY;
+#pragma unroll 4
   for (int c = 0; c < nch; ++c) {
     const float2 ml = part_ml[prow + c];
     if (ml.y > 0.f) M = fmaxf(M, ml.x);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float Ls = 0.f;
+#pragma unroll 4
   for (int c = 0; c < nch; ++c) {
     const float2 ml = part_ml[prow + c];
     if (!(ml.y > 0.f)) continue;
@@ -503,11 +539,12 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
   const int cpart = (pl.NM * BM * 2) / BN;
   long long best = -1;
   int best_nc = 1;
-  const int max_nc = T < 512 ? T : 512;
+  const int max_nc = T < 4096 ? T : 4096;
   for (int nc = 1; nc <= max_nc; ++nc) {
     const int tpc = (T + nc - 1) / nc;
     const int ncr = (T + tpc - 1) / tpc;
     if (ncr != nc) continue;
+    if (tpc * (BN / 16) > kMaxChunkBoxes) continue;  // box ids staged for the smallest pages
     const long long waves = (units * nc + slots - 1) / slots;
     const long long cost = waves * (tpc + c0 + (nc > 1 ? cpart : 0));
     if (best < 0 || cost < best) {

@@ -26,30 +26,53 @@ namespace {
 constexpr int kTopkThreads = 256;
 constexpr int kTreeThreads = 512;
 
-template <int KM>
-__device__ __forceinline__ void topk_insert(float (&vals)[KM], int (&ids)[KM], float v, int i) {
-  if (!better(v, i, vals[KM - 1], ids[KM - 1])) return;
-#pragma unroll
-  for (int j = 0; j < KM; ++j) {
-    const bool b = better(v, i, vals[j], ids[j]);
-    const float tv = vals[j];
-    const int ti = ids[j];
-    vals[j] = b ? v : tv;
-    ids[j] = b ? i : ti;
-    v = b ? tv : v;
-    i = b ? ti : i;
-  }
+// Warp-wide sorted top-k list: lane r < k holds the r-th best (value, index); lanes >= k
+// hold the sentinel (-inf, INT_MAX).  `thr_*` mirror lane k-1 (the current k-th best).
+struct WarpTopk {
+  float v;
+  int i;
+  float thr_v;
+  int thr_i;
+};
+
+__device__ __forceinline__ void wtopk_init(WarpTopk& t) {
+  t.v = -INFINITY;
+  t.i = INT_MAX;
+  t.thr_v = -INFINITY;
+  t.thr_i = INT_MAX;
 }
 
-template <int KM>
-__device__ __forceinline__ void topk_pop(float (&vals)[KM], int (&ids)[KM]) {
-#pragma unroll
-  for (int j = 0; j < KM - 1; ++j) {
-    vals[j] = vals[j + 1];
-    ids[j] = ids[j + 1];
+// Insert (cv, ci) (same value in every lane) into the warp list of length k.
+__device__ __forceinline__ void wtopk_insert(WarpTopk& t, float cv, int ci, int k) {
+  const int lane = threadIdx.x & 31;
+  const unsigned gt = __ballot_sync(0xffffffffu, lane < k && better(cv, ci, t.v, t.i));
+  if (gt == 0u) return;
+  const int pos = __ffs(gt) - 1;  // the list is sorted, so "better than lane r" holds from pos on
+  const float up_v = __shfl_up_sync(0xffffffffu, t.v, 1);
+  const int up_i = __shfl_up_sync(0xffffffffu, t.i, 1);
+  if (lane == pos) {
+    t.v = cv;
+    t.i = ci;
+  } else if (lane > pos && lane < k) {
+    t.v = up_v;
+    t.i = up_i;
   }
-  vals[KM - 1] = -INFINITY;
-  ids[KM - 1] = INT_MAX;
+  t.thr_v = __shfl_sync(0xffffffffu, t.v, k - 1);
+  t.thr_i = __shfl_sync(0xffffffffu, t.i, k - 1);
+}
+
+// Offer one element per lane; the lanes whose element beats the current k-th best are
+// inserted one at a time (after an insertion the threshold rises, so later lanes re-check).
+__device__ __forceinline__ void wtopk_offer(WarpTopk& t, float x, int ix, int k) {
+  unsigned cand = __ballot_sync(0xffffffffu, better(x, ix, t.thr_v, t.thr_i));
+  while (cand) {
+    const int src = __ffs(cand) - 1;
+    const float cv = __shfl_sync(0xffffffffu, x, src);
+    const int ci = __shfl_sync(0xffffffffu, ix, src);
+    wtopk_insert(t, cv, ci, k);
+    cand &= ~(1u << src);
+    cand &= __ballot_sync(0xffffffffu, better(x, ix, t.thr_v, t.thr_i));
+  }
 }
 
 // Best (value, index) across the warp; every lane gets it.
@@ -65,26 +88,9 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
   }
 }
 
-// Pop the k best of the warp's per-lane sorted lists, in order.  Lane r keeps the r-th.
-template <int KM>
-__device__ __forceinline__ void warp_merge_topk(float (&vals)[KM], int (&ids)[KM], int k,
-                                                float& out_v, int& out_i) {
-  const int lane = threadIdx.x & 31;
-  out_v = -INFINITY;
-  out_i = INT_MAX;
-  for (int r = 0; r < k; ++r) {
-    float hv = vals[0];
-    int hi = ids[0];
-    warp_best(hv, hi);
-    if (ids[0] == hi && vals[0] == hv) topk_pop(vals, ids);
-    if (lane == r) {
-      out_v = hv;
-      out_i = hi;
-    }
-  }
-}
-
-template <int KM>
+// One CTA per (draft row, segment).  Each warp streams a contiguous part of the segment
+// (16-byte loads, 4 in flight per lane) through its warp top-k list; warp 0 then folds the
+// other warps' lists into its own and writes the segment's sorted top-k.
 __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
     const float* __restrict__ logp, int V, int seg_len, int S, int k, int vec,
     float* __restrict__ part_v, int* __restrict__ part_i) {
@@ -93,66 +99,58 @@ __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
   const float* x = logp + row * static_cast<long long>(V);
   const int begin = seg * seg_len;
   const int end = min(V, begin + seg_len);
-  float vals[KM];
-  int ids[KM];
-#pragma unroll
-  for (int j = 0; j < KM; ++j) {
-    vals[j] = -INFINITY;
-    ids[j] = INT_MAX;
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kTopkThreads / 32;
+  WarpTopk t;
+  wtopk_init(t);
   if (vec) {
-    // 16-byte loads; 4 in flight per thread per iteration.
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int b4 = begin >> 2, e4 = end >> 2;
-    int i = b4 + threadIdx.x;
-    for (; i + 3 * kTopkThreads < e4; i += 4 * kTopkThreads) {
+    const int per = (e4 - b4 + kWarps - 1) / kWarps;
+    const int wb = b4 + warp * per, we = min(e4, wb + per);
+    for (int i0 = wb; i0 < we; i0 += 4 * 32) {
       float4 a[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = __ldcs(x4 + i + u * kTopkThreads);
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 32 + lane;
+        a[u] = i < we ? __ldcs(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int base = (i + u * kTopkThreads) << 2;
-        topk_insert(vals, ids, a[u].x, base);
-        topk_insert(vals, ids, a[u].y, base + 1);
-        topk_insert(vals, ids, a[u].z, base + 2);
-        topk_insert(vals, ids, a[u].w, base + 3);
+        const int i = i0 + u * 32 + lane;
+        const int base = i < we ? (i << 2) : INT_MAX - 3;
+        wtopk_offer(t, a[u].x, base, k);
+        wtopk_offer(t, a[u].y, base + 1, k);
+        wtopk_offer(t, a[u].z, base + 2, k);
+        wtopk_offer(t, a[u].w, base + 3, k);
       }
     }
-    for (; i < e4; i += kTopkThreads) {
-      const float4 a = __ldcs(x4 + i);
-      const int base = i << 2;
-      topk_insert(vals, ids, a.x, base);
-      topk_insert(vals, ids, a.y, base + 1);
-      topk_insert(vals, ids, a.z, base + 2);
-      topk_insert(vals, ids, a.w, base + 3);
-    }
   } else {
-    for (int i = begin + threadIdx.x; i < end; i += kTopkThreads) topk_insert(vals, ids, __ldcs(x + i), i);
+    const int per = (end - begin + kWarps - 1) / kWarps;
+    const int wb = begin + warp * per, we = min(end, wb + per);
+    for (int i0 = wb; i0 < we; i0 += 32) {
+      const int i = i0 + lane;
+      wtopk_offer(t, i < we ? __ldcs(x + i) : -INFINITY, i < we ? i : INT_MAX, k);
+    }
   }
-
-  __shared__ float s_v[kTopkThreads / 32][KM];
-  __shared__ int s_i[kTopkThreads / 32][KM];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float wv;
-  int wi;
-  warp_merge_topk(vals, ids, k, wv, wi);
-  if (lane < k) {
-    s_v[warp][lane] = wv;
-    s_i[warp][lane] = wi;
-  }
+  __shared__ float s_v[kWarps][32];
+  __shared__ int s_i[kWarps][32];
+  s_v[warp][lane] = t.v;
+  s_i[warp][lane] = t.i;
   __syncthreads();
   if (warp == 0) {
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      const bool have = lane < kTopkThreads / 32 && j < k;
-      vals[j] = have ? s_v[lane][j] : -INFINITY;
-      ids[j] = have ? s_i[lane][j] : INT_MAX;
+    for (int w = 1; w < kWarps; ++w) {
+      for (int r = 0; r < k; ++r) {
+        const float cv = s_v[w][r];
+        const int ci = s_i[w][r];
+        if (!better(cv, ci, t.thr_v, t.thr_i)) break;  // the rest of that list is worse
+        wtopk_insert(t, cv, ci, k);
+      }
     }
-    warp_merge_topk(vals, ids, k, wv, wi);
     if (lane < k) {
       const long long o = (row * S + seg) * k + lane;
-      part_v[o] = wv;
-      part_i[o] = wi;
+      part_v[o] = t.v;
+      part_i[o] = t.i;
     }
   }
 }
@@ -161,12 +159,12 @@ __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
 struct TreeSmem {
   int N;  // candidates
   int off_val, off_key, off_rtok, off_rlp, off_tok, off_lrank, off_sorted, off_flat, off_sel;
-  int off_cntc, off_cnt, off_par, off_err, total;
+  int off_cntc, off_cnt, off_par, off_err, off_stage, off_racc, total;
 };
 
 __host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
 
-__host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, int m) {
+__host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, int m, int S) {
   TreeSmem L;
   L.N = k + (depth - 1) * k * k;
   int o = 0;
@@ -183,6 +181,8 @@ __host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, in
   L.off_cnt = o;    o = align8(o + 4 * (depth + 2));      // selected per layer
   L.off_par = o;    o = align8(o + 4 * m);                // flat parent
   L.off_err = o;    o = align8(o + 4);
+  L.off_racc = o;   o = align8(o + 4 * k * k);            // rank accumulators of one layer
+  L.off_stage = o;  o = align8(o + 8 * (kTreeThreads / 32) * S * k);  // per-warp partial lists
   L.total = o;
   return L;
 }
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     int32_t* __restrict__ tokens, int32_t* __restrict__ parents, int32_t* __restrict__ depth_out,
     uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const TreeSmem L = tree_smem_layout(k, depth, R, m);
+  const TreeSmem L = tree_smem_layout(k, depth, R, m, S);
   double* cV = reinterpret_cast<double*>(smem + L.off_val);
   unsigned long long* ckey = reinterpret_cast<unsigned long long*>(smem + L.off_key);
   int* rtok = reinterpret_cast<int*>(smem + L.off_rtok);
@@ -233,16 +233,24 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
 
   if (tid == 0) *err = 0;
   if (m > 1) {
-    // 1. Merge each row's S sorted segment lists (k each) into the row's top-k.
+    // 1. Merge each row's S sorted segment lists (k each) into the row's top-k.  The
+    //    warp first copies the row's S*k partials to shared memory (independent loads).
+    float* wv = reinterpret_cast<float*>(smem + L.off_stage) + warp * S * k;
+    int* wi = reinterpret_cast<int*>(smem + L.off_stage + 4 * nwarps * S * k) + warp * S * k;
     for (int r = warp; r < R; r += nwarps) {
       const long long base = (static_cast<long long>(b) * R + r) * S * k;
+      for (int e = lane; e < S * k; e += 32) {
+        wv[e] = part_v[base + e];
+        wi[e] = part_i[base + e];
+      }
+      __syncwarp();
       int ptr = 0;
       for (int j = 0; j < k; ++j) {
         float v = -INFINITY;
         int i = INT_MAX;
         if (lane < S && ptr < k) {
-          v = part_v[base + lane * k + ptr];
-          i = part_i[base + lane * k + ptr];
+          v = wv[lane * k + ptr];
+          i = wi[lane * k + ptr];
         }
         float bv = v;
         int bi = i;
@@ -253,6 +261,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           rlp[r * k + j] = bv;
         }
       }
+      __syncwarp();
     }
     for (int x = tid; x < (depth + 1) * k; x += kTreeThreads) cntc[x] = 0;
     for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
@@ -280,16 +289,38 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         ckey[base + t] = order_key(v);
       }
       __syncthreads();
-      // rank inside the layer: value descending, ties -> lower layer-local index
-      for (int t = tid; t < n; t += kTreeThreads) {
-        const unsigned long long kv = ckey[base + t];
-        int rank = 0;
-        for (int y = 0; y < n; ++y) {
-          const unsigned long long ky = ckey[base + y];
-          rank += (ky > kv || (ky == kv && y < t)) ? 1 : 0;
+      // rank inside the layer (value descending, ties -> lower layer-local index).  Layer 1
+      // is the root row's top-k, already in order.  A later layer is k sorted lists (the k
+      // children of each frontier slot, in child-rank order): the rank of child c of slot j
+      // is c plus, for every other slot, the number of its children that come first, found
+      // by a binary search; one thread per (candidate, other slot) pair.
+      if (l == 1) {
+        for (int t = tid; t < n; t += kTreeThreads) {
+          lrank[t] = static_cast<short>(t);
+          sorted[t] = static_cast<short>(t);
         }
-        lrank[base + t] = static_cast<short>(rank);
-        sorted[base + rank] = static_cast<short>(base + t);
+      } else {
+        int* racc = reinterpret_cast<int*>(smem + L.off_racc);
+        for (int t = tid; t < n; t += kTreeThreads) racc[t] = t % k;
+        __syncthreads();
+        for (int q = tid; q < n * k; q += kTreeThreads) {
+          const int t = q / k, j2 = q % k, j = t / k;
+          if (j2 == j) continue;
+          const unsigned long long kv = ckey[base + t];
+          int lo = 0, hi = k;  // children of slot j2 that come before candidate t
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const unsigned long long kw = ckey[base + j2 * k + mid];
+            if (j2 < j ? (kw >= kv) : (kw > kv)) lo = mid + 1; else hi = mid;
+          }
+          if (lo) atomicAdd(&racc[t], lo);
+        }
+        __syncthreads();
+        for (int t = tid; t < n; t += kTreeThreads) {
+          const int rank = racc[t];
+          lrank[base + t] = static_cast<short>(rank);
+          sorted[base + rank] = static_cast<short>(base + t);
+        }
       }
       __syncthreads();
     }
@@ -399,8 +430,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
 
 }  // namespace
 
-// Segments per draft row: enough CTAs to cover the GPU, at most 32 (one per lane of the
-// merge warp), segment length a multiple of 4 (16-byte loads), at least 2048 floats.
+// Segments per draft row: enough CTAs to cover the GPU, at most 8 (the merge stages a
+// row's S*k partials in shared memory), segment length a multiple of 4 (16-byte loads),
+// at least 2048 floats.
 static void build_plan(int B, int V, int k, int depth, int num_sms, int* S_out, int* seg_out) {
   if (num_sms < 1) num_sms = 1;
   const int R = 1 + (depth - 1) * k;
@@ -410,7 +442,7 @@ static void build_plan(int B, int V, int k, int depth, int num_sms, int* S_out, 
   if (want > S) S = static_cast<int>(want);
   const int max_by_len = (V + 2047) / 2048;
   if (S > max_by_len) S = max_by_len;
-  if (S > 32) S = 32;
+  if (S > 8) S = 8;
   if (S < 1) S = 1;
   int seg = (V + S - 1) / S;
   seg = (seg + 3) & ~3;
@@ -442,17 +474,11 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
     const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(draft_logp) % 16 == 0);
     const long long grid = rows * S;
     if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
-#define TS_TOPK(KM)                                                                     \
-  row_topk_kernel<KM><<<static_cast<unsigned>(grid), kTopkThreads, 0, stream>>>(        \
-      draft_logp, V, seg, S, k, vec, part_v, part_i)
-    if (k <= 2) TS_TOPK(2);
-    else if (k <= 4) TS_TOPK(4);
-    else if (k <= 8) TS_TOPK(8);
-    else TS_TOPK(16);
-#undef TS_TOPK
+    row_topk_kernel<<<static_cast<unsigned>(grid), kTopkThreads, 0, stream>>>(draft_logp, V, seg, S, k,
+                                                                              vec, part_v, part_i);
     ++launches;
   }
-  const TreeSmem L = tree_smem_layout(k, depth, R, m);
+  const TreeSmem L = tree_smem_layout(k, depth, R, m, S);
   const int smem = L.total;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
