@@ -165,6 +165,34 @@ int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
                    int32_t* argmax, int32_t* accept_len, int32_t* accept_path, int32_t* bonus,
                    void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * ts_tree_accept_noalloc — ts_tree_accept for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for deployment.
+ *
+ * Who needs it: a serving engine that hands all free HBM to its KV-cache pool at start-up
+ * and allows no later cudaMalloc, a plugin whose host framework owns every device
+ * allocation, or code running while a CUDA graph is captured (no cudaMalloc there).  Such
+ * callers pass only inputs and outputs; the scratch comes from a 1 MiB array compiled into
+ * the library (a file-scope __device__ array that every GPU which loads the library keeps
+ * until the process exits).  No cudaMalloc, cudaFree or allocating library routine is
+ * called.
+ *
+ * Arguments, outputs, ordering rules and device errors are those of ts_tree_accept.
+ * Limit: B * m * S partial (value, index) pairs of 8 bytes must fit in 1 MiB, S being the
+ * number of vocabulary segments per logits row the launch uses (at most ceil(V / 2048);
+ * for example B * m = 512 rows of V = 128256 use S = 2).  Larger requests return
+ * TS_ERR_UNSUPPORTED without launching anything.
+ * The first call on a device looks up the array's device address with that device current
+ * and caches it; make that first call before any stream capture.  All calls share the one
+ * array (its previous contents are irrelevant: every slot is written before it is read), so
+ * calls that may overlap on the GPU (different streams, or different host threads without
+ * ordering) race and must be serialised by the caller.
+ * --------------------------------------------------------------------------------- */
+int ts_tree_accept_noalloc(const void* logits, ts_dtype dt, const int32_t* tokens,
+                           const int32_t* parents, int B, int m, int V,
+                           int32_t* argmax, int32_t* accept_len, int32_t* accept_path,
+                           int32_t* bonus, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@
 //      block max over a packed key, and write the path, its length and the bonus token.
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -270,4 +271,62 @@ int tree_accept_launch(const void* logits, ts_dtype dt, const int32_t* tokens,
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------------------
+// ts_tree_accept_noalloc: tree_accept with its scratch in a fixed device array.
+//
+// Some callers cannot allocate device memory at the moment they verify a tree: a serving
+// engine that hands all free HBM to its KV-cache pool at start-up and forbids later
+// cudaMalloc calls, a plugin hosted by a framework that owns every device allocation, or
+// code that runs inside a region being captured into a CUDA graph.  This variant needs no
+// workspace from them: its scratch (the per-segment partial argmax pairs) lives in the
+// file-scope array below, which every GPU that loads this library keeps until the process
+// exits.  The device address of the array is looked up once per device, on the first call
+// made with that device current, and cached.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB
+__device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return TS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    // In host code the array's name is only a host-side stand-in: the kernels must get the
+    // device address, which the runtime reports for the current device.
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return TS_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TS_OK;
+}
+
+}  // namespace
 }  // namespace ts
+
+extern "C" int ts_tree_accept_noalloc(const void* logits, ts_dtype dt, const int32_t* tokens,
+                                      const int32_t* parents, int B, int m, int V,
+                                      int32_t* argmax, int32_t* accept_len,
+                                      int32_t* accept_path, int32_t* bonus,
+                                      int32_t* dev_status, void* stream) {
+  if (B <= 0 || m <= 0 || V <= 0 || (dt != TS_F32 && dt != TS_BF16)) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
+  if (!logits || !tokens || !parents || !argmax || !accept_len || !accept_path || !bonus)
+    return TS_ERR_INVALID;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  if (ts::tree_accept_workspace_bytes(dt, B, m, V, sms) > ts::kNoAllocScratchBytes)
+    return TS_ERR_UNSUPPORTED;  // the request needs more scratch than the fixed array holds
+  void* scratch = nullptr;
+  const int rc = ts::noalloc_scratch(&scratch);
+  if (rc != TS_OK) return rc;
+  return ts::tree_accept_launch(logits, dt, tokens, parents, B, m, V, argmax, accept_len,
+                                accept_path, bonus, scratch, dev_status,
+                                static_cast<cudaStream_t>(stream), sms);
+}
