@@ -23,7 +23,7 @@
 namespace ts {
 namespace {
 
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 128;
 constexpr int kTreeThreads = 512;
 
 // Warp-wide sorted top-k list: lane r < k holds the r-th best (value, index); lanes >= k
@@ -75,83 +75,65 @@ __device__ __forceinline__ void wtopk_offer(WarpTopk& t, float x, int ix, int k)
   }
 }
 
-// Best (value, index) across the warp; every lane gets it.
-__device__ __forceinline__ void warp_best(float& v, int& i) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
+// Monotone map of a float to an unsigned key (larger value -> larger key, -0 == +0).
+__device__ __forceinline__ unsigned float_order_key(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const unsigned b = __float_as_uint(v);
+  return (b >> 31) ? ~b : (b | 0x80000000u);
 }
 
-// One CTA per (draft row, segment).  Each warp streams a contiguous part of the segment
-// (16-byte loads, 4 in flight per lane) through its warp top-k list; warp 0 then folds the
-// other warps' lists into its own and writes the segment's sorted top-k.
+// One warp per (draft row, segment); a CTA holds kTopkThreads / 32 such warps.  Each warp
+// streams its segment with 16-byte loads (8 in flight per lane) through its warp top-k
+// list.  A lane first tests the maximum of its 4 loaded values against the warp's current
+// k-th best; only then are the 4 values offered one by one, so once the list holds good
+// values an element costs about one comparison.
 __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
-    const float* __restrict__ logp, int V, int seg_len, int S, int k, int vec,
+    const float* __restrict__ logp, int V, int seg_len, int S, int k, int vec, long long items,
     float* __restrict__ part_v, int* __restrict__ part_i) {
-  const long long row = blockIdx.x / S;
-  const int seg = blockIdx.x % S;
+  const int lane = threadIdx.x & 31;
+  const long long item = static_cast<long long>(blockIdx.x) * (kTopkThreads / 32) + (threadIdx.x >> 5);
+  if (item >= items) return;
+  const long long row = item / S;
+  const int seg = static_cast<int>(item % S);
   const float* x = logp + row * static_cast<long long>(V);
   const int begin = seg * seg_len;
   const int end = min(V, begin + seg_len);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kTopkThreads / 32;
   WarpTopk t;
   wtopk_init(t);
   if (vec) {
+    constexpr int U = 8;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int b4 = begin >> 2, e4 = end >> 2;
-    const int per = (e4 - b4 + kWarps - 1) / kWarps;
-    const int wb = b4 + warp * per, we = min(e4, wb + per);
-    for (int i0 = wb; i0 < we; i0 += 4 * 32) {
-      float4 a[4];
+    for (int i0 = b4; i0 < e4; i0 += U * 32) {
+      float4 a[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int i = i0 + u * 32 + lane;
-        a[u] = i < we ? __ldcs(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        a[u] = i < e4 ? __ldcs(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int i = i0 + u * 32 + lane;
-        const int base = i < we ? (i << 2) : INT_MAX - 3;
-        wtopk_offer(t, a[u].x, base, k);
-        wtopk_offer(t, a[u].y, base + 1, k);
-        wtopk_offer(t, a[u].z, base + 2, k);
-        wtopk_offer(t, a[u].w, base + 3, k);
+        const float mx = fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w));
+        const bool hot = i < e4 && mx >= t.thr_v;
+        if (__ballot_sync(0xffffffffu, hot) == 0u) continue;
+        // lanes without a candidate offer the sentinel (-inf, INT_MAX), which never enters
+        wtopk_offer(t, hot ? a[u].x : -INFINITY, hot ? (i << 2) : INT_MAX, k);
+        wtopk_offer(t, hot ? a[u].y : -INFINITY, hot ? (i << 2) + 1 : INT_MAX, k);
+        wtopk_offer(t, hot ? a[u].z : -INFINITY, hot ? (i << 2) + 2 : INT_MAX, k);
+        wtopk_offer(t, hot ? a[u].w : -INFINITY, hot ? (i << 2) + 3 : INT_MAX, k);
       }
     }
   } else {
-    const int per = (end - begin + kWarps - 1) / kWarps;
-    const int wb = begin + warp * per, we = min(end, wb + per);
-    for (int i0 = wb; i0 < we; i0 += 32) {
+    for (int i0 = begin; i0 < end; i0 += 32) {
       const int i = i0 + lane;
-      wtopk_offer(t, i < we ? __ldcs(x + i) : -INFINITY, i < we ? i : INT_MAX, k);
+      wtopk_offer(t, i < end ? __ldcs(x + i) : -INFINITY, i < end ? i : INT_MAX, k);
     }
   }
-  __shared__ float s_v[kWarps][32];
-  __shared__ int s_i[kWarps][32];
-  s_v[warp][lane] = t.v;
-  s_i[warp][lane] = t.i;
-  __syncthreads();
-  if (warp == 0) {
-    for (int w = 1; w < kWarps; ++w) {
-      for (int r = 0; r < k; ++r) {
-        const float cv = s_v[w][r];
-        const int ci = s_i[w][r];
-        if (!better(cv, ci, t.thr_v, t.thr_i)) break;  // the rest of that list is worse
-        wtopk_insert(t, cv, ci, k);
-      }
-    }
-    if (lane < k) {
-      const long long o = (row * S + seg) * k + lane;
-      part_v[o] = t.v;
-      part_i[o] = t.i;
-    }
+  if (lane < k) {
+    const long long o = item * k + lane;
+    part_v[o] = t.v;
+    part_i[o] = t.i;
   }
 }
 
@@ -244,6 +226,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         wi[e] = part_i[base + e];
       }
       __syncwarp();
+      // k rounds: the best head among the S lists (largest value, then lowest id) is taken
+      // with two warp reductions on an order-preserving 32-bit key and the id.
       int ptr = 0;
       for (int j = 0; j < k; ++j) {
         float v = -INFINITY;
@@ -252,13 +236,16 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           v = wv[lane * k + ptr];
           i = wi[lane * k + ptr];
         }
-        float bv = v;
-        int bi = i;
-        warp_best(bv, bi);
-        if (lane < S && ptr < k && i == bi && v == bv) ++ptr;
+        const unsigned key = float_order_key(v);
+        const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+        const int imin = __reduce_min_sync(0xffffffffu, key == kmax ? i : INT_MAX);
+        const bool win = key == kmax && i == imin;
+        const int wl = __ffs(__ballot_sync(0xffffffffu, win)) - 1;
+        const float best_v = __shfl_sync(0xffffffffu, v, wl < 0 ? 0 : wl);
+        if (lane < S && ptr < k && win) ++ptr;
         if (lane == 0) {
-          rtok[r * k + j] = bi;
-          rlp[r * k + j] = bv;
+          rtok[r * k + j] = imin;
+          rlp[r * k + j] = best_v;
         }
       }
       __syncwarp();
@@ -287,6 +274,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         ctok[base + t] = tok;
         cV[base + t] = v;
         ckey[base + t] = order_key(v);
+        if (l > 1) reinterpret_cast<int*>(smem + L.off_racc)[t] = t % k;
       }
       __syncthreads();
       // rank inside the layer (value descending, ties -> lower layer-local index).  Layer 1
@@ -301,8 +289,6 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         }
       } else {
         int* racc = reinterpret_cast<int*>(smem + L.off_racc);
-        for (int t = tid; t < n; t += kTreeThreads) racc[t] = t % k;
-        __syncthreads();
         for (int q = tid; q < n * k; q += kTreeThreads) {
           const int t = q / k, j2 = q % k, j = t / k;
           if (j2 == j) continue;
@@ -430,19 +416,19 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
 
 }  // namespace
 
-// Segments per draft row: enough CTAs to cover the GPU, at most 8 (the merge stages a
-// row's S*k partials in shared memory), segment length a multiple of 4 (16-byte loads),
-// at least 2048 floats.
+// Segments per draft row (one warp each): at least 8 warps per SM when the rows allow it,
+// at most 32 (one per lane of the merging warp), segment length a multiple of 4 (16-byte
+// loads) and at least 1024 floats.
 static void build_plan(int B, int V, int k, int depth, int num_sms, int* S_out, int* seg_out) {
   if (num_sms < 1) num_sms = 1;
   const int R = 1 + (depth - 1) * k;
   const long long rows = static_cast<long long>(B) * R;
   int S = (V + 16383) / 16384;
-  const long long want = (2LL * num_sms + rows - 1) / rows;
+  const long long want = (8LL * num_sms + rows - 1) / rows;
   if (want > S) S = static_cast<int>(want);
-  const int max_by_len = (V + 2047) / 2048;
+  const int max_by_len = (V + 1023) / 1024;
   if (S > max_by_len) S = max_by_len;
-  if (S > 8) S = 8;
+  if (S > 32) S = 32;
   if (S < 1) S = 1;
   int seg = (V + S - 1) / S;
   seg = (seg + 3) & ~3;
@@ -472,10 +458,10 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
   int launches = 0;
   if (m > 1) {
     const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(draft_logp) % 16 == 0);
-    const long long grid = rows * S;
+    const long long grid = (rows * S + kTopkThreads / 32 - 1) / (kTopkThreads / 32);
     if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
     row_topk_kernel<<<static_cast<unsigned>(grid), kTopkThreads, 0, stream>>>(draft_logp, V, seg, S, k,
-                                                                              vec, part_v, part_i);
+                                                                              vec, rows * S, part_v, part_i);
     ++launches;
   }
   const TreeSmem L = tree_smem_layout(k, depth, R, m, S);
