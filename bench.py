@@ -307,6 +307,8 @@ def run_ours(args, rank, world, dev):
                         (("tree_build", t_build), ("tree_attention", t_attn), ("tree_accept", t_acc))},
         "algorithmic_bytes": ab,
         "attention_tflops": round(attention_flops(w, inp["prefix_len"].tolist()) / (attn_ms * 1e-3) / 1e12, 2),
+        "attention_plan": ts.tree_attention_plan(step.d["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix,
+                                                 workloads.BLOCK_SIZE),
         "clocks": clocks,
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "kernel": "tree_attention (tcgen05 kernel + split-K combine)",

@@ -140,6 +140,15 @@ int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, t
                       float scale, void* out, float* lse,
                       void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Launch plan ts_tree_attention would use for these sizes on the current device (a
+ * diagnostic; the pages have no counterpart).  Writes 5 ints to plan_out: [0] path (0 =
+ * CUDA-core, 1 = tensor-core), [1] M tiles of 128 rows per CTA, [2] chunks per (sequence, KV
+ * head, row group), [3] 64-key tiles per chunk, [4] split mode (0 = one chunk, 1 = chunks
+ * merged inside a thread-block cluster, 2 = chunks merged through the workspace).  Returns
+ * TS_OK or the validation error ts_tree_attention would return. */
+int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                           int block_size, int* plan_out);
+
 /* ------------------------------------------------------------------------------------
  * ts_tree_accept — greedy verification of the tree.
  * Source: "lesty.tech — EAGLE-2 vs. Medusa", section 4 (greedy: a draft token is accepted iff

@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "TreeSpecError", "library", "library_path", "launch_count", "status_string",
     "tree_build", "tree_attention", "tree_accept", "new_status", "check_status",
-    "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace",
+    "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace", "tree_attention_plan",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +63,8 @@ def library():
         L.ts_tree_attention_workspace.argtypes = [I, I, I, I, I, I, I]
         L.ts_tree_attention.restype = I
         L.ts_tree_attention.argtypes = [P, P, P, I, I, I, P, I, P, I, P, I, I, I, I, I, F, P, P, P, S, P, P]
+        L.ts_tree_attention_plan.restype = I
+        L.ts_tree_attention_plan.argtypes = [I, I, I, I, I, I, I, I, P]
         L.ts_tree_accept_workspace.restype = S
         L.ts_tree_accept_workspace.argtypes = [I, I, I, I]
         L.ts_tree_accept.restype = I
@@ -146,6 +148,17 @@ def tree_attention_workspace(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: i
                              max_prefix: int) -> int:
     dt = TS_F32 if dtype == torch.float32 else TS_BF16
     return int(library().ts_tree_attention_workspace(dt, B, m, Hq, Hkv, d, max_prefix))
+
+
+def tree_attention_plan(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: int, d: int, max_prefix: int,
+                        block_size: int) -> Dict[str, int]:
+    """The launch plan tree_attention uses for these sizes on the current device."""
+    dt = TS_F32 if dtype == torch.float32 else TS_BF16
+    out = (ctypes.c_int * 5)()
+    _check(library().ts_tree_attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, out))
+    modes = {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}
+    return {"path": "tensor-core" if out[0] else "cuda-core", "m_tiles": out[1], "chunks": out[2],
+            "tiles_per_chunk": out[3], "split": modes.get(out[4], str(out[4]))}
 
 
 def tree_accept_workspace(dtype: torch.dtype, B: int, m: int, V: int) -> int:

@@ -99,6 +99,24 @@ size_t ts_tree_attention_workspace(ts_dtype dt, int B, int m, int Hq, int Hkv, i
   return 256;
 }
 
+int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                           int block_size, int* plan_out) {
+  const int rc = ts::check_attention(dt, B, m, Hq, Hkv, d, max_prefix);
+  if (rc != TS_OK) return rc;
+  if (!plan_out || block_size <= 0) return TS_ERR_INVALID;
+  if (!ts::attention_uses_tc(dt, d, block_size)) {
+    plan_out[0] = 0;
+    plan_out[1] = 0;
+    plan_out[2] = 1;
+    plan_out[3] = 0;
+    plan_out[4] = 0;
+    return TS_OK;
+  }
+  plan_out[0] = 1;
+  ts::attention_tc_plan(B, m, Hq, Hkv, max_prefix, ts::device_sm_count(), plan_out + 1);
+  return TS_OK;
+}
+
 int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, ts_dtype dt,
                       int num_blocks, int block_size, const int32_t* block_table,
                       int max_blocks, const int32_t* prefix_len, int max_prefix,

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
   if (i < m) {
     float bv = -INFINITY;
     int bi = INT_MAX;
+#pragma unroll 4
     for (int s = 0; s < S; ++s) upd(bv, bi, part_v[(r0 + i) * S + s], part_i[(r0 + i) * S + s]);
     s_amax[i] = bi;
     argmax[r0 + i] = bi;

@@ -8,30 +8,42 @@
 // Work unit: (sequence b, KV head, row group, chunk of 64-key tiles).  The g query heads
 // that share a KV head and the m tree nodes are packed into GEMM rows, row = node*g +
 // head-in-group, so every K/V byte fetched from HBM serves m*g query rows on the tensor
-// cores.  A row group is one or two 128-row M tiles (NM).
+// cores.  A row group is one (NM = 1) or two (NM = 2) 128-row M tiles.  One CTA per SM.
 //
-// Warp roles (one CTA, 128*(1+NM) + 128 threads):
-//   warp 0      TMA producer: per 64-key tile, one box of min(block_size,64) rows x 64
-//               bf16 (128-byte swizzle) per page and head-dim half for K and for V, from the
-//               block table; positions past the sequence come from an out-of-range block
-//               (zero fill).  STAGES-deep ring, full/empty mbarriers.
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer:
+// Warp roles (128*(1+NM) + 128 threads):
+//   warp 0      stages the chunk's physical block ids in shared memory, then one thread is
+//               the TMA producer: per 64-key tile one box of min(block_size,64) rows x 64
+//               bf16 (128-byte swizzle) per page and head-dim half, for K and for V on
+//               separate mbarriers; positions past the sequence load an out-of-range block
+//               (zero fill).  STAGES-deep ring.
+//   warp 1      TMEM allocator + the single thread that issues tcgen05.mma:
 //                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
 //                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
-//               issued ping-pong over the M tiles so one tile's softmax overlaps the other
-//               tile's MMAs; completion is signalled with tcgen05.commit.
 //   warps 4..   softmax, one thread per row (TMEM lane): load S, apply the tree mask on the
 //               tiles that reach the tree, online softmax in the log2 domain with lazy
 //               rescaling of O (only when the running max grows by more than 2^8), write P
-//               as bf16 into TMEM, then the epilogue (O / l, or an fp32 partial for the
-//               split-K combine).
-// TMEM columns: O_i at 128*i, S_i at 128*NM + 64*i, P_i at 192*NM + 32*i.  P never aliases
-// S, so the next S = Q K^T can run while the previous P V still reads P; a softmax pass
-// starts only after the commit that covers both the new S and the previous P V.
+//               as bf16 into TMEM; then the epilogue.
+// Overlap: with one M tile, S and P are double-buffered in TMEM (S = Q K^T of tile t+2 runs
+// while tile t's softmax runs); with two M tiles the MMAs of one tile run during the
+// other tile's softmax.  P never aliases S.
+// TMEM columns: O_i at 128*i; S_{i,s} at 128*NM + 64*(i*SB + s); P_{i,s} after the S
+// buffers, 32 columns each.
+// Split over chunks of one (sequence, KV head, row group):
+//   direct   one chunk: the epilogue writes O / l.
+//   cluster  the chunks are the CTAs of one thread-block cluster (<= 8): each CTA parks its
+//            fp32 O rows and (max, sum) in its shared memory, and after a cluster barrier
+//            every CTA merges a slice of the rows by reading all CTAs' shared memory
+//            (distributed shared memory) and writes the output: no partials in HBM and no
+//            second launch.
+//   global   more chunks than a cluster holds: fp32 partials go to the workspace and
+//            combine_kernel merges them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -49,21 +61,33 @@ constexpr uint32_t KHALF = BN * 128;   // 64 keys x 64 bf16 = 8 KB
 constexpr uint32_t KTILE = 2 * KHALF;  // 16 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxChunkBoxes = 2048;       // physical-block ids a CTA stages in shared memory
+constexpr int kMaxCluster = 8;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+enum Mode { kDirect = 0, kCluster = 1, kGlobal = 2 };
 
 template <int NM>
 struct Cfg {
-  static constexpr int STAGES = NM == 1 ? 2 : 4;
+  static constexpr int SB = NM == 1 ? 2 : 1;  // S / P buffers per M tile
+  static constexpr int STAGES = NM == 1 ? 5 : 4;
   static constexpr int THREADS = 128 + 128 * NM;
-  static constexpr int MIN_BLOCKS = NM == 1 ? 2 : 1;  // two single-tile CTAs share an SM
-  static constexpr uint32_t TMEM_COLS = NM == 1 ? 256 : 512;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S = 128 * NM;
+  static constexpr uint32_t COL_P = COL_S + 64 * NM * SB;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = NM * QTILE;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KTILE;
-  static constexpr int NBAR = 4 * STAGES + 3 * NM;
+  // full_k[ST] full_v[ST] empty_k[ST] empty_v[ST] s_full[NM*SB] p_full[NM*SB] o_ready[NM] o_final[NM]
+  // (p_full is per S buffer: with two buffers a fast softmax warp may reach tile t+1 while
+  // slower warps of its M tile still work on tile t, and their arrivals must not mix)
+  static constexpr int NBAR = 4 * STAGES + 2 * NM * SB + 2 * NM;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t OFF_BLK = OFF_MISC + 16;
-  static constexpr uint32_t SMEM_BYTES = OFF_BLK + 4 * kMaxChunkBoxes + 1024;  // + 1 KB alignment slack
+  static constexpr uint32_t OFF_ML = OFF_MISC + 16;            // (max, sum) per row, cluster merge
+  static constexpr uint32_t OFF_BLK = OFF_ML + NM * BM * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_BLK + 4 * kMaxChunkBoxes + 1024;  // + alignment slack
+  static_assert(COL_P + 32 * NM * SB <= TMEM_COLS, "TMEM budget");
+  static_assert(2 * STAGES * KTILE >= NM * BM * 512, "O rows must fit in the K/V ring for the merge");
 };
 
 struct Params {
@@ -76,7 +100,7 @@ struct Params {
   float* part_o;
   float2* part_ml;
   int32_t* status;
-  int m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk;
+  int m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk, mode;
   float scale_log2;
 };
 
@@ -89,12 +113,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Byte offset of 16-byte chunk c of parked O row R (rows of 512 B; the chunk index is
+// XOR-swizzled with the row so a warp writing 32 rows spreads over all banks).
+__device__ __forceinline__ uint32_t orow_off(int R, int c) {
+  return static_cast<uint32_t>(R) * 512u + (static_cast<uint32_t>(c ^ (R & 31)) << 4);
+}
+
 template <int NM>
-__global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
+__global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const Params p) {
   using C = Cfg<NM>;
   constexpr int ST = C::STAGES;
+  constexpr int SB = C::SB;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -104,6 +135,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   const int rg = blockIdx.x, chunk = blockIdx.y, bk = blockIdx.z;
   const int b = bk / p.Hkv, kvh = bk % p.Hkv;
   const int L = p.prefix_len[b];
+  // (the whole cluster shares b, so every CTA of a cluster returns here together)
   if (L < 0 || L > p.max_prefix) {
     if (threadIdx.x == 0 && rg == 0 && chunk == 0) report(p.status, TS_ERR_DEVICE_CHECK);
     return;
@@ -111,9 +143,11 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   const int nkeys = L + p.m;
   const int T = (nkeys + BN - 1) / BN;
   const int t0 = chunk * p.tpc;
-  if (t0 >= T) return;
-  const int nt = min(p.tpc, T - t0);
+  if (t0 >= T && p.mode != kCluster) return;
+  const int nt = t0 < T ? min(p.tpc, T - t0) : 0;  // 0: an idle CTA of a cluster
   const int nchunks_b = (T + p.tpc - 1) / p.tpc;
+  // a sequence that fits in one chunk is written directly also in the global mode
+  const bool direct = p.mode == kDirect || (p.mode == kGlobal && nchunks_b == 1);
   const int R0 = rg * NM * BM;
   const int rows_here = min(p.rows - R0, NM * BM);
   const int nma = (rows_here + BM - 1) / BM;
@@ -123,11 +157,13 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   auto full_v = [&](int s) { return bar(ST + s); };
   auto empty_k = [&](int s) { return bar(2 * ST + s); };
   auto empty_v = [&](int s) { return bar(3 * ST + s); };
-  auto s_full = [&](int i) { return bar(4 * ST + i); };
-  auto p_full = [&](int i) { return bar(4 * ST + NM + i); };
-  auto o_final = [&](int i) { return bar(4 * ST + 2 * NM + i); };
+  auto s_full = [&](int i, int sb) { return bar(4 * ST + i * SB + sb); };
+  auto p_full = [&](int i, int sb) { return bar(4 * ST + NM * SB + i * SB + sb); };
+  auto o_ready = [&](int i) { return bar(4 * ST + 2 * NM * SB + i); };
+  auto o_final = [&](int i) { return bar(4 * ST + 2 * NM * SB + NM + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + C::OFF_MISC + 4);
+  float2* s_ml = reinterpret_cast<float2*>(sptr + C::OFF_ML);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -137,8 +173,11 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
       mbar_init(empty_v(s), 1);
     }
     for (int i = 0; i < NM; ++i) {
-      mbar_init(s_full(i), 1);
-      mbar_init(p_full(i), 128);
+      for (int sb = 0; sb < SB; ++sb) {
+        mbar_init(s_full(i, sb), 1);
+        mbar_init(p_full(i, sb), 128);
+      }
+      mbar_init(o_ready(i), 1);
       mbar_init(o_final(i), 1);
     }
     *abort_flag = 0;
@@ -149,8 +188,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
     tmem_relinquish();
   }
   // Q rows of this row group -> shared memory in the 128-byte-swizzled K-major layout
-  // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.
-  // (loads are issued in batches of 4 per thread so their latencies overlap)
+  // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.  Loads
+  // are issued in batches of 4 per thread so their latencies overlap.
   for (int c0 = threadIdx.x; c0 < NM * BM * 16; c0 += 4 * C::THREADS) {
     uint4 v[4];
 #pragma unroll
@@ -159,7 +198,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
       const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
       const int grow = R0 + row;
       v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (c < NM * BM * 16 && grow < p.rows) {
+      if (nt > 0 && c < NM * BM * 16 && grow < p.rows) {
         const int node = grow / p.g, head = kvh * p.g + grow % p.g;
         const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
         v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + off));
@@ -212,6 +251,10 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // per-row softmax state, kept for the epilogue
+  float m_ref = -INFINITY, l_sum = 0.f;
+  bool ok = true;
+
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
@@ -226,10 +269,10 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
           if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) goto producer_done;
           mbar_expect_tx(fb, KTILE);
           const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
+          const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
           for (int j = 0; j < bpt; ++j) {
             const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
             const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
-            const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
             tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
             tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
           }
@@ -244,78 +287,82 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
+    if (lane == 0 && nt > 0) {
       constexpr uint32_t idq = idesc_bf16_f32(128, BN, 0, 0);
       constexpr uint32_t idp = idesc_bf16_f32(128, HD, 0, 1);
-      auto tS = [&](int i) { return tmem + 128u * NM + 64u * i; };
       auto tO = [&](int i) { return tmem + 128u * i; };
-      auto tP = [&](int i) { return tmem + 192u * NM + 32u * i; };
-      auto qk = [&](int i, int s) {
+      auto tS = [&](int i, int sb) { return tmem + C::COL_S + 64u * (i * SB + sb); };
+      auto tP = [&](int i, int sb) { return tmem + C::COL_P + 32u * (i * SB + sb); };
+      auto qk = [&](int i, int s, int sb) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t h = kk >> 2, ko = (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + i * QTILE + h * QHALF + ko, 16, 1024);
           const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + s * KTILE + h * KHALF + ko, 16, 1024);
-          mma_ss(tS(i), a, bd, idq, kk > 0 ? 1u : 0u);
+          mma_ss(tS(i, sb), a, bd, idq, kk > 0 ? 1u : 0u);
         }
-        tc_commit(s_full(i));
+        tc_commit(s_full(i, sb));
       };
-      auto pv = [&](int i, int s, bool first) {
+      auto pv = [&](int i, int s, int sb, bool first) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           // B = V tile, MN-major: 64 head-dim columns per 128-byte row, 8-key groups 1 KB
           // apart (stride offset), the second head-dim half KHALF further (leading offset).
           const uint64_t bd = sdesc_sw128(sbase + C::OFF_V + s * KTILE + kk * 2048, KHALF, 1024);
-          mma_ts(tO(i), tP(i) + 8u * kk, bd, idp, (first && kk == 0) ? 0u : 1u);
+          mma_ts(tO(i), tP(i, sb) + 8u * kk, bd, idp, (first && kk == 0) ? 0u : 1u);
         }
       };
-      bool ok = mbar_wait(full_k(0), 0, abort_flag, p.status);
-      if (ok) {
+      bool mok = true;
+      for (int t = 0; mok && t < SB && t < nt; ++t) {
+        mok = mbar_wait(full_k(t % ST), (t / ST) & 1, abort_flag, p.status);
+        if (!mok) break;
         tc_fence_after();
-        for (int i = 0; i < nma; ++i) qk(i, 0);
-        tc_commit(empty_k(0));
+        for (int i = 0; i < nma; ++i) qk(i, t % ST, t % SB);
+        tc_commit(empty_k(t % ST));
       }
-      for (int t = 0; ok && t < nt; ++t) {
+      for (int t = 0; mok && t < nt; ++t) {
         const int s = t % ST;
-        ok = mbar_wait(full_v(s), (t / ST) & 1, abort_flag, p.status);
-        if (!ok) break;
+        mok = mbar_wait(full_v(s), (t / ST) & 1, abort_flag, p.status);
+        if (!mok) break;
         tc_fence_after();
+        const int tn = t + SB;
         for (int i = 0; i < nma; ++i) {
-          ok = mbar_wait(p_full(i), t & 1, abort_flag, p.status);
-          if (!ok) break;
+          mok = mbar_wait(p_full(i, t % SB), (t / SB) & 1, abort_flag, p.status);
+          if (!mok) break;
           tc_fence_after();
-          pv(i, s, t == 0);
-          if (t + 1 < nt) {
-            const int s1 = (t + 1) % ST;
+          pv(i, s, t % SB, t == 0);
+          tc_commit(o_ready(i));
+          if (tn < nt) {
             if (i == 0) {
-              ok = mbar_wait(full_k(s1), ((t + 1) / ST) & 1, abort_flag, p.status);
-              if (!ok) break;
+              mok = mbar_wait(full_k(tn % ST), (tn / ST) & 1, abort_flag, p.status);
+              if (!mok) break;
               tc_fence_after();
             }
-            qk(i, s1);
-            if (i == nma - 1) tc_commit(empty_k(s1));
+            qk(i, tn % ST, tn % SB);
+            if (i == nma - 1) tc_commit(empty_k(tn % ST));
           }
         }
-        if (!ok) break;
+        if (!mok) break;
         tc_commit(empty_v(s));
       }
       for (int i = 0; i < nma; ++i) tc_commit(o_final(i));
-      if (!ok) {
+      if (!mok) {
         for (int i = 0; i < nma; ++i) drain_wait(o_final(i), 0);
       }
     }
+    __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------ softmax + epilogue ------------------------------
+    // ------------------------------ softmax ------------------------------
     const int i = (warp - 4) >> 2;
     const int q4 = warp & 3;
-    if (i < nma) {
+    if (i < nma && nt > 0) {
       const int r = q4 * 32 + lane;
       const int grow = R0 + i * BM + r;
       const bool valid = grow < p.rows;
       const int node = valid ? grow / p.g : 0;
-      const int head = kvh * p.g + (valid ? grow % p.g : 0);
       uint64_t mw0 = 0, mw1 = 0, mw2 = 0, mw3 = 0;
       if (valid) {
         const uint64_t* mrow = p.mask + (static_cast<long long>(b) * p.m + node) * p.W;
@@ -326,13 +373,12 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
       }
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t tO = tmem + lane_off + 128u * i;
-      const uint32_t tS = tmem + lane_off + 128u * NM + 64u * i;
-      const uint32_t tP = tmem + lane_off + 192u * NM + 32u * i;
       const float sl2 = p.scale_log2;
-      float m_ref = -INFINITY, l_sum = 0.f;
-      bool ok = true;
       for (int t = 0; t < nt; ++t) {
-        ok = mbar_wait_warp(s_full(i), t & 1, abort_flag, p.status);
+        const int sb = t % SB;
+        const uint32_t tS = tmem + lane_off + C::COL_S + 64u * (i * SB + sb);
+        const uint32_t tP = tmem + lane_off + C::COL_P + 32u * (i * SB + sb);
+        ok = mbar_wait_warp(s_full(i, sb), (t / SB) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         float s[BN];
@@ -389,6 +435,10 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
         l_sum += rs;
         tmem_st32(tP, pk);
         if (__any_sync(0xffffffffu, resc)) {
+          // O must hold P V of tile t-1 before it is rescaled
+          ok = mbar_wait_warp(o_ready(i), (t - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
@@ -415,12 +465,13 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
           fence_proxy_async_smem();
         }
         tc_fence_before();
-        mbar_arrive(p_full(i));
+        mbar_arrive(p_full(i, sb));
       }
       if (ok) ok = mbar_wait_warp(o_final(i), 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
-        if (nchunks_b == 1) {
+        const int head = kvh * p.g + (valid ? grow % p.g : 0);
+        if (direct) {
           const float inv = (valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
           __nv_bfloat16* dst = p.out + ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD;
 #pragma unroll 1
@@ -440,9 +491,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
             }
           }
           if (valid && p.lse != nullptr)
-            p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] =
-                (m_ref + log2f(l_sum)) * 0.69314718055994530942f;
-        } else {
+            p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (m_ref + log2f(l_sum)) * kLn2;
+        } else if (p.mode == kGlobal) {
           const long long prow = (static_cast<long long>(bk) * p.rows + grow) * p.nchunk + chunk;
           float* dst = p.part_o + prow * HD;
 #pragma unroll 1
@@ -458,9 +508,77 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
             }
           }
           if (valid) p.part_ml[prow] = make_float2(m_ref, l_sum);
+        } else {
+          // cluster: park O (fp32) in the now idle K/V ring and (max, sum) in OFF_ML
+          const int Rl = i * BM + r;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * cc, o);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              *reinterpret_cast<uint4*>(sptr + C::OFF_K + orow_off(Rl, cc * 8 + v4)) =
+                  make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+          }
         }
       }
     }
+  }
+
+  if (p.mode == kCluster) {
+    // rows without a valid partial from this CTA advertise an empty sum
+    if (warp >= 4) {
+      const int i = (warp - 4) >> 2;
+      const int Rl = i * BM + (warp & 3) * 32 + lane;
+      const bool have = ok && i < nma && nt > 0 && R0 + Rl < p.rows;
+      s_ml[Rl] = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    // merge: CTA q of the cluster owns rows [q*NM*BM/cs, (q+1)*NM*BM/cs) of the row group;
+    // one warp per row, lane c reads 16-byte chunk c of the row from every CTA.
+    const int cs = p.nchunk;
+    const int q = static_cast<int>(cluster_ctarank());
+    const int per = (NM * BM + cs - 1) / cs;
+    const int r_begin = q * per, r_end = min(NM * BM, r_begin + per);
+    const uint32_t ml_local = sbase + C::OFF_ML;
+    const uint32_t o_local = sbase + C::OFF_K;
+    for (int Rl = r_begin + warp; Rl < r_end; Rl += C::THREADS / 32) {
+      const int grow = R0 + Rl;
+      if (grow >= p.rows) break;
+      float M = -INFINITY;
+      float2 mls[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        mls[c] = make_float2(-INFINITY, 0.f);
+        if (c < cs) mls[c] = ld_dsmem_f2(dsmem_addr(ml_local + 8u * Rl, c));
+        if (mls[c].y > 0.f) M = fmaxf(M, mls[c].x);
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float Ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        if (!(mls[c].y > 0.f)) continue;
+        const float w = ex2_approx(mls[c].x - M);
+        Ls += w * mls[c].y;
+        const float4 o = ld_dsmem_f4(dsmem_addr(o_local + orow_off(Rl, lane), c));
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const int node = grow / p.g, head = kvh * p.g + grow % p.g;
+      const long long oo = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + lane * 4;
+      uint2 w2;
+      w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(p.out + oo) = w2;
+      if (lane == 0 && p.lse != nullptr)
+        p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (M + log2f(Ls)) * kLn2;
+    }
+    // nobody leaves while another CTA may still read its shared memory
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -471,8 +589,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, Cfg<NM>::MIN_BLOCKS)
   }
 }
 
-// Split-K merge: one warp per (sequence, KV head, row); rows of sequences that fit in one
-// chunk were written directly by the attention kernel and are skipped.
+// Split-K merge for the global mode: one warp per (sequence, KV head, row); rows of
+// sequences that fit in one chunk were written directly by the attention kernel.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
                                                       const float2* __restrict__ part_ml,
                                                       const int32_t* __restrict__ prefix_len,
@@ -516,14 +634,56 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   w.y = pack_bf16x2(acc.z * inv, acc.w * inv);
   *reinterpret_cast<uint2*>(p.out + oo) = w;
   if (lane == 0 && p.lse != nullptr)
-    p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] =
-        (M + log2f(Ls)) * 0.69314718055994530942f;
+    p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (M + log2f(Ls)) * kLn2;
+}
+
+template <int NM>
+static cudaError_t set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(tree_attn_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<NM>::SMEM_BYTES);
+  });
+  return err;
+}
+
+// How many clusters of `cs` CTAs (one per SM) the device runs at once; 0 if unknown.
+template <int NM>
+static int active_clusters(int cs) {
+  static std::mutex mu;
+  static int cache[kMaxCluster + 1] = {};
+  static bool done[kMaxCluster + 1] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[cs]) return cache[cs];
+  done[cs] = true;
+  if (set_smem_attr<NM>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, cs, 1);
+  cfg.blockDim = dim3(Cfg<NM>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<NM>::SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 1;
+  attr.val.clusterDim.y = cs;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tree_attn_tc_kernel<NM>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[cs] = n;
+  return n;
 }
 
 struct Plan {
-  int NM, rowgroups, nc, tpc;
+  int NM, rowgroups, nc, tpc, mode;
 };
 
+// Makespan model in 64-key-tile units: waves x (tiles per CTA + fixed cost per CTA) plus,
+// for the global mode, the partial write/read and the combine launch.
 static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms) {
   Plan pl;
   if (num_sms < 1) num_sms = 1;
@@ -532,28 +692,73 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
   pl.rowgroups = (rows + pl.NM * BM - 1) / (pl.NM * BM);
   const int T = (max_prefix + m + BN - 1) / BN;
   const long long units = static_cast<long long>(B) * Hkv * pl.rowgroups;
-  const long long slots = static_cast<long long>(num_sms) * (pl.NM == 1 ? 2 : 1);
-  // makespan model in tile units: waves x (tiles per chunk + fixed cost per CTA); a split
-  // adds the partial write + combine read of the CTA's rows (in 64-key-tile equivalents)
   const int c0 = 3;
-  const int cpart = (pl.NM * BM * 2) / BN;
+  const int rows_cta = rows < pl.NM * BM ? rows : pl.NM * BM;
+  const int cglob = 4 + (rows_cta * 2 + BN - 1) / BN;
   long long best = -1;
-  int best_nc = 1;
+  pl.nc = 1;
+  pl.tpc = T;
+  pl.mode = kDirect;
   const int max_nc = T < 4096 ? T : 4096;
   for (int nc = 1; nc <= max_nc; ++nc) {
     const int tpc = (T + nc - 1) / nc;
-    const int ncr = (T + tpc - 1) / tpc;
-    if (ncr != nc) continue;
+    if ((T + tpc - 1) / tpc != nc) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;  // box ids staged for the smallest pages
-    const long long waves = (units * nc + slots - 1) / slots;
-    const long long cost = waves * (tpc + c0 + (nc > 1 ? cpart : 0));
+    const long long waves = (units * nc + num_sms - 1) / num_sms;
+    const long long cost = waves * (tpc + c0) + (nc > 1 ? waves * cglob : 0);
     if (best < 0 || cost < best) {
       best = cost;
-      best_nc = nc;
+      pl.nc = nc;
+      pl.tpc = tpc;
+      pl.mode = nc > 1 ? kGlobal : kDirect;
     }
   }
-  pl.nc = best_nc;
-  pl.tpc = (T + best_nc - 1) / best_nc;
+  // Optional override for tests and tuning: TREESPEC_ATTN_SPLIT=direct | cluster:N | global:N
+  // (ignored when the requested split is not feasible for these sizes).
+  if (const char* ov = std::getenv("TREESPEC_ATTN_SPLIT")) {
+    int n = 0;
+    if (std::strcmp(ov, "direct") == 0) {
+      if (T * (BN / 16) <= kMaxChunkBoxes) {
+        pl.nc = 1;
+        pl.tpc = T;
+        pl.mode = kDirect;
+        return pl;
+      }
+    } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n) {
+      const int tpc = (T + n - 1) / n;
+      const int act = pl.NM == 1 ? active_clusters<1>(n) : active_clusters<2>(n);
+      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && act > 0) {
+        pl.nc = n;
+        pl.tpc = tpc;
+        pl.mode = kCluster;
+        return pl;
+      }
+    } else if (std::sscanf(ov, "global:%d", &n) == 1 && n >= 2 && n <= T) {
+      const int tpc = (T + n - 1) / n;
+      if (tpc * (BN / 16) <= kMaxChunkBoxes) {
+        pl.nc = (T + tpc - 1) / tpc;
+        pl.tpc = tpc;
+        pl.mode = pl.nc > 1 ? kGlobal : kDirect;
+        return pl;
+      }
+    }
+  }
+  for (int cs = 2; cs <= kMaxCluster; cs *= 2) {
+    if (T < cs) break;
+    const int tpc = (T + cs - 1) / cs;
+    if ((T + tpc - 1) / tpc != cs) continue;
+    if (tpc * (BN / 16) > kMaxChunkBoxes) continue;
+    const int act = pl.NM == 1 ? active_clusters<1>(cs) : active_clusters<2>(cs);
+    if (act <= 0) continue;
+    const long long waves = (units + act - 1) / act;
+    const long long cost = waves * (tpc + c0 + 1);
+    if (cost < best) {
+      best = cost;
+      pl.nc = cs;
+      pl.tpc = tpc;
+      pl.mode = kCluster;
+    }
+  }
   return pl;
 }
 
@@ -623,17 +828,22 @@ static bool cached_kv_map(CUtensorMap* out, const void* base, int num_blocks, in
 template <int NM>
 static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, const Plan& pl,
                      int B, int Hkv, cudaStream_t stream) {
-  using C = Cfg<NM>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(tree_attn_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return TS_ERR_CUDA;
-  dim3 grid(pl.rowgroups, pl.nc, B * Hkv);
-  tree_attn_tc_kernel<NM><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, prm);
-  return TS_OK;
+  if (set_smem_attr<NM>() != cudaSuccess) return TS_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.rowgroups, pl.nc, B * Hkv);
+  cfg.blockDim = dim3(Cfg<NM>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<NM>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  if (pl.mode == kCluster) {
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = pl.nc;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<NM>, mk, mv, prm) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
 }  // namespace tc
@@ -645,9 +855,17 @@ bool attention_uses_tc(ts_dtype dt, int d, int block_size) {
 
 size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms) {
   const tc::Plan pl = tc::make_plan(B, m, Hq, Hkv, max_prefix, num_sms);
-  if (pl.nc <= 1) return 256;
+  if (pl.mode != tc::kGlobal) return 256;
   const size_t prow = static_cast<size_t>(B) * Hkv * m * (Hq / Hkv) * pl.nc;
   return prow * tc::HD * 4 + prow * 8 + 512;
+}
+
+void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4) {
+  const tc::Plan pl = tc::make_plan(B, m, Hq, Hkv, max_prefix, num_sms);
+  out4[0] = pl.NM;
+  out4[1] = pl.nc;
+  out4[2] = pl.tpc;
+  out4[3] = pl.mode;
 }
 
 int attention_tc_launch(const AttnArgs& a, int num_sms) {
@@ -676,16 +894,18 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   prm.max_prefix = a.max_prefix;
   prm.tpc = pl.tpc;
   prm.nchunk = pl.nc;
+  prm.mode = pl.mode;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   const size_t prow = static_cast<size_t>(a.B) * a.Hkv * prm.rows * pl.nc;
-  prm.part_o = pl.nc > 1 ? static_cast<float*>(a.workspace) : nullptr;
-  prm.part_ml = pl.nc > 1 ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * tc::HD * 4)
-                          : nullptr;
+  prm.part_o = pl.mode == tc::kGlobal ? static_cast<float*>(a.workspace) : nullptr;
+  prm.part_ml = pl.mode == tc::kGlobal
+                    ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * tc::HD * 4)
+                    : nullptr;
   const int rc = pl.NM == 1 ? tc::launch_nm<1>(mk, mv, prm, pl, a.B, a.Hkv, a.stream)
                             : tc::launch_nm<2>(mk, mv, prm, pl, a.B, a.Hkv, a.stream);
   if (rc != TS_OK) return rc;
   int launches = 1;
-  if (pl.nc > 1) {
+  if (pl.mode == tc::kGlobal) {
     const int total_rows = a.B * a.Hkv * prm.rows;
     tc::combine_kernel<<<(total_rows + 7) / 8, 256, 0, a.stream>>>(prm.part_o, prm.part_ml, a.prefix_len,
                                                                    prm, total_rows);

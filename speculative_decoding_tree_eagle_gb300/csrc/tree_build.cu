@@ -221,9 +221,25 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     int* wi = reinterpret_cast<int*>(smem + L.off_stage + 4 * nwarps * S * k) + warp * S * k;
     for (int r = warp; r < R; r += nwarps) {
       const long long base = (static_cast<long long>(b) * R + r) * S * k;
-      for (int e = lane; e < S * k; e += 32) {
-        wv[e] = part_v[base + e];
-        wi[e] = part_i[base + e];
+      for (int e0 = lane; e0 < S * k; e0 += 8 * 32) {  // 8 independent loads in flight
+        float v8[8];
+        int i8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = e0 + 32 * u;
+          if (e < S * k) {
+            v8[u] = part_v[base + e];
+            i8[u] = part_i[base + e];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = e0 + 32 * u;
+          if (e < S * k) {
+            wv[e] = v8[u];
+            wi[e] = i8[u];
+          }
+        }
       }
       __syncwarp();
       // k rounds: the best head among the S lists (largest value, then lowest id) is taken

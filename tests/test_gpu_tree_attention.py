@@ -138,3 +138,35 @@ def test_workloads_full_size_sampled(name):
     tree = oracle_tree(inp, w)
     sel = sample_rows(w, np.random.default_rng(w.seed))
     _run(inp, w, tree["mask"], tree["mask_words"], select=sel)
+
+
+SPLITS = [("direct", 0), ("cluster:2", 1), ("cluster:4", 1), ("cluster:8", 1), ("global:3", 2), ("global:11", 2)]
+ROW_CASES = [dict(B=2, Hq=8, Hkv=2, m=30, k=5, depth=6),      # 120 rows: one M tile, double-buffered S
+             dict(B=1, Hq=16, Hkv=4, m=60, k=8, depth=6)]     # 240 rows: two M tiles
+
+
+@pytest.mark.parametrize("rows_case", ROW_CASES, ids=["one_m_tile", "two_m_tiles"])
+@pytest.mark.parametrize("split,mode", SPLITS, ids=[s for s, _ in SPLITS])
+def test_every_split_mode_repeated_calls(split, mode, rows_case, monkeypatch):
+    """Force each way of splitting a sequence over CTAs (one chunk, chunks merged inside a
+    cluster, chunks merged through the workspace) with chunks long enough to wrap the K/V
+    ring several times; five calls in a row must agree exactly and match the oracle."""
+    lib()
+    monkeypatch.setenv("TREESPEC_ATTN_SPLIT", split)
+    w, inp, tree = _small("attn_split", prefix=(1900, 1900), **rows_case)
+    plan = ts.tree_attention_plan(inp["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix, 16)
+    assert plan["split"] == {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}[mode], plan
+    g = {k: inp[k].to(dev()) for k in ("q", "k_cache", "v_cache", "block_table", "prefix_len")}
+    first = None
+    for _ in range(5):
+        status = ts.new_status(dev())
+        out, _ = ts.tree_attention(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["prefix_len"],
+                                   words_i64(tree["mask_words"]), max_prefix=w.max_prefix, status=status)
+        ts.check_status(status)
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)
+    ref, _ = oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
+                                   inp["prefix_len"].numpy(), tree["mask"], scale_of(w))
+    assert_attention_close(first, ref, torch.bfloat16)
