@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefix", type=int, default=None,
+                    help="override the workload's prefix length (a smaller case for detailed profiling; "
+                         "the JSON line then names the modified workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch through the API each step instead of "
@@ -205,12 +208,20 @@ class Step:
         self.accept()
 
 
+def get_workload(args):
+    w = workloads.WORKLOADS[args.workload]
+    if args.prefix is not None:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}_prefix{args.prefix}", prefix=(args.prefix, args.prefix))
+    return w
+
+
 def run_ours(args, rank, world, dev):
     import speculative_decoding_tree_eagle_gb300 as ts
     from speculative_decoding_tree_eagle_gb300 import build as tsbuild
     tsbuild.build()
     ts.library()
-    w = workloads.WORKLOADS[args.workload]
+    w = get_workload(args)
     inp = workloads.generate(w)
     step = Step(w, inp, dev)
     if w.plant_frac > 0:
@@ -395,7 +406,7 @@ def cpu_baseline(w, inp, budget_s=12.0):
 
 
 def run_reference(args, rank, world):
-    w = workloads.WORKLOADS[args.workload]
+    w = get_workload(args)
     inp = workloads.generate(w)
     ab = algo_bytes(w, inp["prefix_len"].tolist())
     heads = pick_heads(w)

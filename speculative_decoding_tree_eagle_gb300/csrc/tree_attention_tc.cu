@@ -11,11 +11,11 @@
 // cores.  A row group is one (NM = 1) or two (NM = 2) 128-row M tiles.  One CTA per SM.
 //
 // Warp roles (128*(1+NM) + 128 threads):
-//   warp 0      stages the chunk's physical block ids in shared memory, then one thread is
-//               the TMA producer: per 64-key tile one box of min(block_size,64) rows x 64
-//               bf16 (128-byte swizzle) per page and head-dim half, for K and for V on
-//               separate mbarriers; positions past the sequence load an out-of-range block
-//               (zero fill).  STAGES-deep ring.
+//   warps 0, 2  warp 0 stages the chunk's physical block ids in shared memory; then one
+//               thread of warp 0 loads the K tiles and one thread of warp 2 the V tiles with
+//               TMA: per 64-key tile one box of min(block_size,64) rows x 64 bf16 (128-byte
+//               swizzle) per page and head-dim half, on separate mbarriers; positions past
+//               the sequence load an out-of-range block (zero fill).  STAGES-deep ring.
 //   warp 1      TMEM allocator + the single thread that issues tcgen05.mma:
 //                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
 //                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
@@ -255,36 +255,34 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
   bool ok = true;
 
-  if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
+  if (warp == 0 || warp == 2) {
+    // ------------------------------ TMA producers ------------------------------
+    // K tiles from warp 0, V tiles from warp 2: a TMA instruction holds its issuing thread
+    // for a while, so two issuing warps double the rate of small (page-sized) boxes.
     if (lane == 0) {
+      const int kv = warp == 0 ? 0 : 1;
+      const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % ST;
         const uint32_t ph = (t / ST) & 1;
         const int key0 = (t0 + t) * BN;
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
-          const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
-          if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) goto producer_done;
-          mbar_expect_tx(fb, KTILE);
-          const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
-          const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
-          for (int j = 0; j < bpt; ++j) {
-            const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
-            const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
-            tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
-            tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
-          }
+        const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
+        const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
+        if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) break;
+        mbar_expect_tx(fb, KTILE);
+        const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
+        for (int j = 0; j < bpt; ++j) {
+          const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
+          const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
+          tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
+          tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
         }
         issued = t + 1;
       }
-    producer_done:
       if (*abort_flag) {
-        for (int t = max(0, issued - ST); t < issued; ++t) {
-          drain_wait(full_k(t % ST), (t / ST) & 1);
-          drain_wait(full_v(t % ST), (t / ST) & 1);
-        }
+        for (int t = max(0, issued - ST); t < issued; ++t)
+          drain_wait(kv == 0 ? full_k(t % ST) : full_v(t % ST), (t / ST) & 1);
       }
     }
     __syncwarp();
