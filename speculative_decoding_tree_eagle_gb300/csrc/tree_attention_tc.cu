@@ -10,12 +10,13 @@
 // head-in-group, so every K/V byte fetched from HBM serves m*g query rows on the tensor
 // cores.  A row group is one (NM = 1) or two (NM = 2) 128-row M tiles.  One CTA per SM.
 //
-// Warp roles (128*(1+NM) + 128 threads):
-//   warps 0, 2  warp 0 stages the chunk's physical block ids in shared memory; then one
-//               thread of warp 0 loads the K tiles and one thread of warp 2 the V tiles with
-//               TMA: per 64-key tile one box of min(block_size,64) rows x 64 bf16 (128-byte
-//               swizzle) per page and head-dim half, on separate mbarriers; positions past
-//               the sequence load an out-of-range block (zero fill).  STAGES-deep ring.
+// Warp roles (128*(1+NM) + 128 + 32 threads):
+//   warps 0,2,3,last  warp 0 stages the chunk's physical block ids in shared memory; then
+//               one thread in each of four warps issues TMA loads (K: warps 0 and 3, V: warp
+//               2 and the last warp, half of each tile's boxes each): per 64-key tile one box
+//               of min(block_size,64) rows x 64 bf16 (128-byte swizzle) per page and
+//               head-dim half; positions past the sequence load an out-of-range block (zero
+//               fill).  STAGES-deep ring; each full barrier expects both producers.
 //   warp 1      TMEM allocator + the single thread that issues tcgen05.mma:
 //                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
 //                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
@@ -30,11 +31,12 @@
 // buffers, 32 columns each.
 // Split over chunks of one (sequence, KV head, row group):
 //   direct   one chunk: the epilogue writes O / l.
-//   cluster  the chunks are the CTAs of one thread-block cluster (<= 8): each CTA parks its
-//            fp32 O rows and (max, sum) in its shared memory, and after a cluster barrier
-//            every CTA merges a slice of the rows by reading all CTAs' shared memory
-//            (distributed shared memory) and writes the output: no partials in HBM and no
-//            second launch.
+//   cluster  the chunks are the CTAs of one thread-block cluster (<= 8): after a cluster
+//            barrier each CTA stores its fp32 O rows and (max, sum) straight into the shared
+//            memory of the CTA that owns those rows (distributed shared memory), and after a
+//            second barrier every owner merges its rows locally and writes the output: no
+//            partials in HBM and no second launch.
+// Chunks are balanced: chunk c of a sequence of T tiles covers [c*T/nc, (c+1)*T/nc).
 //   global   more chunks than a cluster holds: fp32 partials go to the workspace and
 //            combine_kernel merges them.
 #include <cuda.h>
@@ -70,7 +72,11 @@ template <int NM>
 struct Cfg {
   static constexpr int SB = NM == 1 ? 2 : 1;  // S / P buffers per M tile
   static constexpr int STAGES = NM == 1 ? 5 : 4;
-  static constexpr int THREADS = 128 + 128 * NM;
+  // one-tile groups are bandwidth-bound and get a fourth TMA-issuing warp; two-tile groups
+  // stay at 12 warps to keep 170 registers per thread
+  static constexpr int THREADS = 128 + 128 * NM + (NM == 1 ? 32 : 0);
+  static constexpr int EXTRA_WARP = 4 + 4 * NM;  // == THREADS / 32 when there is no extra warp
+  static constexpr int V_PRODUCERS = NM == 1 ? 2 : 1;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 128 * NM;
   static constexpr uint32_t COL_P = COL_S + 64 * NM * SB;
@@ -142,12 +148,12 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   }
   const int nkeys = L + p.m;
   const int T = (nkeys + BN - 1) / BN;
-  const int t0 = chunk * p.tpc;
-  if (t0 >= T && p.mode != kCluster) return;
-  const int nt = t0 < T ? min(p.tpc, T - t0) : 0;  // 0: an idle CTA of a cluster
-  const int nchunks_b = (T + p.tpc - 1) / p.tpc;
-  // a sequence that fits in one chunk is written directly also in the global mode
-  const bool direct = p.mode == kDirect || (p.mode == kGlobal && nchunks_b == 1);
+  // balanced chunks: chunk c covers tiles [c*T/nc, (c+1)*T/nc) of this sequence
+  const int t0 = static_cast<int>(static_cast<long long>(chunk) * T / p.nchunk);
+  const int nt = static_cast<int>(static_cast<long long>(chunk + 1) * T / p.nchunk) - t0;
+  if (nt == 0 && p.mode != kCluster) return;  // (an idle CTA of a cluster still merges)
+  // a sequence whose tiles all fall into one chunk is written directly also in the global mode
+  const bool direct = p.mode == kDirect || (p.mode == kGlobal && min(T, p.nchunk) == 1);
   const int R0 = rg * NM * BM;
   const int rows_here = min(p.rows - R0, NM * BM);
   const int nma = (rows_here + BM - 1) / BM;
@@ -167,8 +173,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
-      mbar_init(full_k(s), 1);
-      mbar_init(full_v(s), 1);
+      mbar_init(full_k(s), 2);  // each producer warp registers its own bytes
+      mbar_init(full_v(s), C::V_PRODUCERS);
       mbar_init(empty_k(s), 1);
       mbar_init(empty_v(s), 1);
     }
@@ -255,13 +261,18 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
   bool ok = true;
 
-  if (warp == 0 || warp == 2) {
+  if (warp == 0 || warp == 2 || warp == 3 || warp == C::EXTRA_WARP) {
     // ------------------------------ TMA producers ------------------------------
-    // K tiles from warp 0, V tiles from warp 2: a TMA instruction holds its issuing thread
-    // for a while, so two issuing warps double the rate of small (page-sized) boxes.
+    // A TMA instruction holds its issuing thread for a while, so page-sized boxes are issued
+    // from several warps: K tiles by warps 0 and 3 (half of each tile's boxes each), V tiles
+    // by warp 2, and for one-tile groups also by the extra warp (again half each).
     if (lane == 0) {
-      const int kv = warp == 0 ? 0 : 1;
+      const int kv = (warp == 0 || warp == 3) ? 0 : 1;
+      const int part = (warp == 0 || warp == 2) ? 0 : 1;
+      const int nparts = kv == 0 ? 2 : C::V_PRODUCERS;
       const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
+      const int nbox = 2 * bpt;                    // boxes per tile: pages x head-dim halves
+      const int b_begin = part * (nbox / 2), b_end = (part == 0 && nparts == 2) ? nbox / 2 : nbox;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % ST;
@@ -270,13 +281,13 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
         const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
         if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(fb, KTILE);
+        mbar_expect_tx(fb, static_cast<uint32_t>(b_end - b_begin) * rpb * 128);
         const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
-        for (int j = 0; j < bpt; ++j) {
+        for (int e = b_begin; e < b_end; ++e) {
+          const int j = e >> 1, h = e & 1;      // page j of the tile, head-dim half h
           const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
           const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
-          tma_load_4d(dst0 + j * rpb * 128, map, fb, 0, rin, kvh, blk);
-          tma_load_4d(dst0 + KHALF + j * rpb * 128, map, fb, 64, rin, kvh, blk);
+          tma_load_4d(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk);
         }
         issued = t + 1;
       }
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < C::EXTRA_WARP) {
     // ------------------------------ softmax ------------------------------
     const int i = (warp - 4) >> 2;
     const int q4 = warp & 3;
@@ -506,50 +517,60 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
             }
           }
           if (valid) p.part_ml[prow] = make_float2(m_ref, l_sum);
-        } else {
-          // cluster: park O (fp32) in the now idle K/V ring and (max, sum) in OFF_ML
-          const int Rl = i * BM + r;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32u * cc, o);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              *reinterpret_cast<uint4*>(sptr + C::OFF_K + orow_off(Rl, cc * 8 + v4)) =
-                  make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
-          }
         }
+        // cluster mode: O stays in TMEM until every CTA of the cluster has left its loop
       }
     }
   }
 
   if (p.mode == kCluster) {
-    // rows without a valid partial from this CTA advertise an empty sum
-    if (warp >= 4) {
+    // Merge through distributed shared memory.  Rows of the row group are split evenly over
+    // the cs CTAs ("owners"); slot (c, row) of an owner's receive area holds CTA c's partial.
+    // 1) barrier: every CTA has left its loop, so all K/V rings are idle and reusable;
+    // 2) every CTA pushes its (max, sum) and fp32 O rows into the owners' rings with remote
+    //    stores (no round trips); 3) barrier: all pushes are visible; 4) each owner merges
+    //    its rows from local shared memory and writes the output.
+    const int cs = p.nchunk;
+    const int q = static_cast<int>(cluster_ctarank());
+    const int per = NM * BM / cs;  // cs divides 128
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp >= 4 && warp < C::EXTRA_WARP) {
       const int i = (warp - 4) >> 2;
       const int Rl = i * BM + (warp & 3) * 32 + lane;
       const bool have = ok && i < nma && nt > 0 && R0 + Rl < p.rows;
-      s_ml[Rl] = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+      const int owner = Rl / per;
+      const int slot = q * per + (Rl - owner * per);
+      const float2 ml = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+      st_dsmem_f2(dsmem_addr(sbase + C::OFF_ML + 8u * slot, owner), ml);
+      if (__any_sync(0xffffffffu, have)) {  // tcgen05.ld is warp-wide
+        tc_fence_after();
+        const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 128u * i;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32u * cc, o);
+          if (have) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              st_dsmem_u4(dsmem_addr(sbase + C::OFF_K + orow_off(slot, cc * 8 + v4), owner),
+                          make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]));
+          }
+        }
+      }
     }
-    tc_fence_before();
     cluster_sync_all();
-    // merge: CTA q of the cluster owns rows [q*NM*BM/cs, (q+1)*NM*BM/cs) of the row group;
-    // one warp per row, lane c reads 16-byte chunk c of the row from every CTA.
-    const int cs = p.nchunk;
-    const int q = static_cast<int>(cluster_ctarank());
-    const int per = (NM * BM + cs - 1) / cs;
-    const int r_begin = q * per, r_end = min(NM * BM, r_begin + per);
-    const uint32_t ml_local = sbase + C::OFF_ML;
-    const uint32_t o_local = sbase + C::OFF_K;
-    for (int Rl = r_begin + warp; Rl < r_end; Rl += C::THREADS / 32) {
+    // owner merge: one warp per row, lane c handles 16-byte chunk c of the row
+    const float2* ml_local = reinterpret_cast<const float2*>(sptr + C::OFF_ML);
+    for (int rr = warp; rr < per; rr += C::THREADS / 32) {
+      const int Rl = q * per + rr;
       const int grow = R0 + Rl;
       if (grow >= p.rows) break;
       float M = -INFINITY;
       float2 mls[kMaxCluster];
 #pragma unroll
       for (int c = 0; c < kMaxCluster; ++c) {
-        mls[c] = make_float2(-INFINITY, 0.f);
-        if (c < cs) mls[c] = ld_dsmem_f2(dsmem_addr(ml_local + 8u * Rl, c));
+        mls[c] = c < cs ? ml_local[c * per + rr] : make_float2(-INFINITY, 0.f);
         if (mls[c].y > 0.f) M = fmaxf(M, mls[c].x);
       }
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         if (!(mls[c].y > 0.f)) continue;
         const float w = ex2_approx(mls[c].x - M);
         Ls += w * mls[c].y;
-        const float4 o = ld_dsmem_f4(dsmem_addr(o_local + orow_off(Rl, lane), c));
+        const float4 o = *reinterpret_cast<const float4*>(sptr + C::OFF_K + orow_off(c * per + rr, lane));
         acc.x += w * o.x;
         acc.y += w * o.y;
         acc.z += w * o.z;
@@ -575,8 +596,6 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
       if (lane == 0 && p.lse != nullptr)
         p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (M + log2f(Ls)) * kLn2;
     }
-    // nobody leaves while another CTA may still read its shared memory
-    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -601,19 +620,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int L = prefix_len[b];
   if (L < 0 || L > p.max_prefix) return;
   const int T = (L + p.m + BN - 1) / BN;
-  const int nch = (T + p.tpc - 1) / p.tpc;
-  if (nch <= 1) return;
-  const long long prow = static_cast<long long>(wid) * p.nchunk;
+  const int nc = p.nchunk;
+  if (min(T, nc) <= 1) return;  // written directly by the attention kernel
+  const long long prow = static_cast<long long>(wid) * nc;
+  // chunk c holds tiles [c*T/nc, (c+1)*T/nc); empty chunks wrote nothing
+  auto empty = [&](int c) {
+    return static_cast<long long>(c + 1) * T / nc == static_cast<long long>(c) * T / nc;
+  };
   float M = -INFINITY;
 #pragma unroll 4
-  for (int c = 0; c < nch; ++c) {
+  for (int c = 0; c < nc; ++c) {
+    if (empty(c)) continue;
     const float2 ml = part_ml[prow + c];
     if (ml.y > 0.f) M = fmaxf(M, ml.x);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float Ls = 0.f;
 #pragma unroll 4
-  for (int c = 0; c < nch; ++c) {
+  for (int c = 0; c < nc; ++c) {
+    if (empty(c)) continue;
     const float2 ml = part_ml[prow + c];
     if (!(ml.y > 0.f)) continue;
     const float w = exp2f(ml.x - M);
