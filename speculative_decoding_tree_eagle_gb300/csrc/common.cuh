@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <utility>
 
 #include "treespec.h"
 
@@ -38,6 +39,36 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// ---------------------------------------------------------------------------------
+// programmatic dependent launch: every library kernel is launched with programmatic stream
+// serialization and waits for the previous grid (whatever it was) before it reads any input,
+// so its launch and CTA placement overlap the previous kernel's tail.  Only kernels whose grid
+// is a handful of CTAs (tree_kernel, accept_kernel) or whose dependent is one (the argmax
+// stream, followed by accept_kernel) let the next grid in at their start: CTAs of a dependent
+// grid that sit waiting next to a wide, still-running grid slowed it down measurably (a draft
+// row stream followed by tree_kernel took 7-26 us longer), so wide kernels trigger at exit.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------------

@@ -65,6 +65,8 @@ __device__ __forceinline__ void block_best(float& v, int& i) {
 __global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
     const __nv_bfloat16* __restrict__ logits, int V, int seg_len, int S, int vec,
     float* __restrict__ part_v, int* __restrict__ part_i) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long row = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const __nv_bfloat16* x = logits + row * static_cast<long long>(V);
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
 __global__ void __launch_bounds__(kArgThreads) argmax_f32_kernel(
     const float* __restrict__ logits, int V, int seg_len, int S, int vec,
     float* __restrict__ part_v, int* __restrict__ part_i) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long row = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const float* x = logits + row * static_cast<long long>(V);
@@ -154,6 +158,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
   __shared__ int s_par[TS_MAX_NODES];
   __shared__ int s_tok[TS_MAX_NODES];
   __shared__ unsigned s_key[32];
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
   const long long r0 = static_cast<long long>(b) * m;
   bool bad = false;
@@ -259,15 +265,15 @@ int tree_accept_launch(const void* logits, ts_dtype dt, const int32_t* tokens,
   if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
   if (dt == TS_BF16) {
     const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    argmax_bf16_kernel<<<static_cast<unsigned>(grid), kArgThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(logits), V, seg, S, vec, part_v, part_i);
+    launch_pdl(argmax_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(kArgThreads), 0, stream,
+               static_cast<const __nv_bfloat16*>(logits), V, seg, S, vec, part_v, part_i);
   } else {
     const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    argmax_f32_kernel<<<static_cast<unsigned>(grid), kArgThreads, 0, stream>>>(
-        static_cast<const float*>(logits), V, seg, S, vec, part_v, part_i);
+    launch_pdl(argmax_f32_kernel, dim3(static_cast<unsigned>(grid)), dim3(kArgThreads), 0, stream,
+               static_cast<const float*>(logits), V, seg, S, vec, part_v, part_i);
   }
-  accept_kernel<<<B, kAcceptThreads, 0, stream>>>(part_v, part_i, S, tokens, parents, m, argmax,
-                                                   accept_len, accept_path, bonus, dev_status);
+  launch_pdl(accept_kernel, dim3(B), dim3(kAcceptThreads), 0, stream, part_v, part_i, S, tokens, parents, m,
+             argmax, accept_len, accept_path, bonus, dev_status);
   count_launches(2);
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

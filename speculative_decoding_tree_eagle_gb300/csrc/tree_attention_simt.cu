@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) tree_attn_simt_kernel(
     int max_prefix, const uint64_t* __restrict__ mask, int m, int Hq, int Hkv, int d, int bs,
     int num_blocks, float scale, T* __restrict__ out, float* __restrict__ lse, int32_t* status) {
   constexpr int DPL = 8;  // up to 256 / 32 head-dim elements per lane
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = Hq / Hkv, kh = h / g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,13 +109,13 @@ __global__ void __launch_bounds__(kSimtWarps * 32) tree_attn_simt_kernel(
 int attention_simt_launch(const AttnArgs& a) {
   dim3 grid(a.Hq, a.B);
   if (a.dt == TS_F32) {
-    tree_attn_simt_kernel<float><<<grid, kSimtWarps * 32, 0, a.stream>>>(
+    launch_pdl(tree_attn_simt_kernel<float>, grid, dim3(kSimtWarps * 32), 0, a.stream,
         static_cast<const float*>(a.q), static_cast<const float*>(a.k_cache),
         static_cast<const float*>(a.v_cache), a.block_table, a.max_blocks, a.prefix_len,
         a.max_prefix, a.mask, a.m, a.Hq, a.Hkv, a.d, a.block_size, a.num_blocks, a.scale,
         static_cast<float*>(a.out), a.lse, a.dev_status);
   } else {
-    tree_attn_simt_kernel<__nv_bfloat16><<<grid, kSimtWarps * 32, 0, a.stream>>>(
+    launch_pdl(tree_attn_simt_kernel<__nv_bfloat16>, grid, dim3(kSimtWarps * 32), 0, a.stream,
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),
         static_cast<const __nv_bfloat16*>(a.v_cache), a.block_table, a.max_blocks, a.prefix_len,
         a.max_prefix, a.mask, a.m, a.Hq, a.Hkv, a.d, a.block_size, a.num_blocks, a.scale,

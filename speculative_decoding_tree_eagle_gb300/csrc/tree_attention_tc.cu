@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = blockIdx.x, chunk = blockIdx.y, bk = blockIdx.z;
   const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  pdl_wait();
   const int L = p.prefix_len[b];
   // (the whole cluster shares b, so every CTA of a cluster returns here together)
   if (L < 0 || L > p.max_prefix) {
@@ -612,6 +613,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float2* __restrict__ part_ml,
                                                       const int32_t* __restrict__ prefix_len,
                                                       Params p, int total_rows) {
+  pdl_wait();
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= total_rows) return;
@@ -857,14 +859,17 @@ static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params&
   cfg.blockDim = dim3(Cfg<NM>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<NM>::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (pl.mode == kCluster) {
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 1;
-    attr.val.clusterDim.y = pl.nc;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = pl.nc;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<NM>, mk, mv, prm) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
@@ -930,8 +935,9 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   int launches = 1;
   if (pl.mode == tc::kGlobal) {
     const int total_rows = a.B * a.Hkv * prm.rows;
-    tc::combine_kernel<<<(total_rows + 7) / 8, 256, 0, a.stream>>>(prm.part_o, prm.part_ml, a.prefix_len,
-                                                                   prm, total_rows);
+    if (launch_pdl(tc::combine_kernel, dim3((total_rows + 7) / 8), dim3(256), 0, a.stream, prm.part_o,
+                   prm.part_ml, a.prefix_len, prm, total_rows) != cudaSuccess)
+      return TS_ERR_CUDA;
     ++launches;
   }
   count_launches(launches);

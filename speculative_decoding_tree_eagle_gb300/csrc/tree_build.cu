@@ -5,11 +5,10 @@
 // Medusa", section 5 for the parent-walk mask.
 //
 // Two launches:
-//   1. row_topk_kernel — the HBM stream.  Every draft row [V] fp32 is split into S
-//      segments; one CTA per (row, segment) keeps a per-thread sorted top-k in registers
-//      while streaming the segment with 16-byte loads, then merges its 256 lists to one
-//      top-k with warp shuffles.  Partials go to the workspace.
-//   2. tree_kernel — one CTA per sequence, all on chip: merge each row's S partial lists,
+//   1. row_topk_kernel — the HBM stream.  One CTA per draft row [V] fp32, one warp per
+//      segment; the warps share lower bounds of the row's k-th best so that almost every
+//      element costs one comparison, and the row's top-k goes to the workspace.
+//   2. tree_kernel — one CTA per sequence, all on chip: read each row's top-k,
 //      expand layer by layer (value = parent value + log-prob, fp64, root -> leaf order),
 //      pick each layer's frontier by rank, rerank every candidate with per-layer binary
 //      searches, flatten by (depth, parent position, child rank), and build each node's
@@ -23,7 +22,6 @@
 namespace ts {
 namespace {
 
-constexpr int kTopkThreads = 128;
 constexpr int kTreeThreads = 512;
 
 // Warp-wide sorted top-k list: lane r < k holds the r-th best (value, index); lanes >= k
@@ -75,65 +73,203 @@ __device__ __forceinline__ void wtopk_offer(WarpTopk& t, float x, int ix, int k)
   }
 }
 
-// Monotone map of a float to an unsigned key (larger value -> larger key, -0 == +0).
+// Monotone map of a float to an unsigned key (larger value -> larger key, -0 == +0), and back
+// (the inverse returns +0 for both zeros).
 __device__ __forceinline__ unsigned float_order_key(float v) {
   if (v == 0.0f) v = 0.0f;
   const unsigned b = __float_as_uint(v);
   return (b >> 31) ? ~b : (b | 0x80000000u);
 }
+__device__ __forceinline__ float key_to_float(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
-// One warp per (draft row, segment); a CTA holds kTopkThreads / 32 such warps.  Each warp
-// streams its segment with 16-byte loads (8 in flight per lane) through its warp top-k
-// list.  A lane first tests the maximum of its 4 loaded values against the warp's current
-// k-th best; only then are the 4 values offered one by one, so once the list holds good
-// values an element costs about one comparison.
-__global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
-    const float* __restrict__ logp, int V, int seg_len, int S, int k, int vec, long long items,
-    float* __restrict__ part_v, int* __restrict__ part_i) {
-  const int lane = threadIdx.x & 31;
-  const long long item = static_cast<long long>(blockIdx.x) * (kTopkThreads / 32) + (threadIdx.x >> 5);
-  if (item >= items) return;
-  const long long row = item / S;
-  const int seg = static_cast<int>(item % S);
+// 64-bit candidate key: value key in the high word, 0xffffffff - index in the low word, so that
+// "larger key" is exactly better() (larger value, then smaller index).  0 = no candidate.
+__device__ __forceinline__ unsigned long long cand_key(float v, int i) {
+  return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+         (0xffffffffu - static_cast<unsigned>(i));
+}
+
+// Merge the n (<= 32) keys buf[0..n) into the warp's sorted key list lk (lane r < k holds the
+// r-th best, 0 beyond): every key's rank in the union is counted, the k best are scattered
+// through `scratch` (k slots) and read back.
+__device__ __forceinline__ unsigned long long merge_keys(unsigned long long lk,
+                                                         const unsigned long long* buf, int n, int k,
+                                                         unsigned long long* scratch, int lane) {
+  const unsigned long long ck = lane < n ? buf[lane] : 0ull;
+  int rc = 0, rl = lane;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) {
+    const unsigned long long o = __shfl_sync(0xffffffffu, ck, j);
+    rc += o > ck;
+    rl += o > lk;
+  }
+  for (int j = 0; j < k; ++j) rc += __shfl_sync(0xffffffffu, lk, j) > ck;
+  if (lane < k) scratch[lane] = 0ull;
+  __syncwarp();
+  if (ck != 0ull && rc < k) scratch[rc] = ck;
+  if (lane < k && lk != 0ull && rl < k) scratch[rl] = lk;
+  __syncwarp();
+  const unsigned long long r = lane < k ? scratch[lane] : 0ull;
+  __syncwarp();
+  return r;
+}
+
+// The J largest of the 32 lanes' keys (0 = none), in order; lane 0 stores them to dst.
+__device__ __forceinline__ unsigned warp_kth_key(unsigned key, int J, unsigned* dst, int lane) {
+  unsigned top = 0u;
+  for (int j = 0; j < J; ++j) {
+    top = __reduce_max_sync(0xffffffffu, key);
+    const unsigned holders = __ballot_sync(0xffffffffu, key == top);
+    if (lane == __ffs(holders) - 1) key = 0u;
+    if (dst != nullptr && lane == 0) dst[j] = top;
+  }
+  return top;
+}
+
+// Four consecutive elements 4q..4q+3 of a row; positions at or past `end` read -inf.
+template <bool VEC>
+__device__ __forceinline__ float4 load_quad(const float* __restrict__ x, int q, int end) {
+  const float4 neg = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  if (VEC) return 4 * q < end ? __ldcs(reinterpret_cast<const float4*>(x) + q) : neg;
+  const int e = 4 * q;
+  return make_float4(e < end ? __ldcs(x + e) : -INFINITY, e + 1 < end ? __ldcs(x + e + 1) : -INFINITY,
+                     e + 2 < end ? __ldcs(x + e + 2) : -INFINITY, e + 3 < end ? __ldcs(x + e + 3) : -INFINITY);
+}
+
+// One CTA per draft row, one warp per segment of seg_len elements (a multiple of 4).  Each warp
+// streams its segment four elements per lane at a time, U quads per lane per batch with the
+// next batch's loads in flight while the current one is examined, and keeps a sorted warp
+// top-k list.  An element is examined only if it can still reach the row's top-k: three lower
+// bounds of the row's k-th best value are shared through shared memory,
+//   (a) the k-th largest of all warps' top-J lane maxima over their first batch (J = ceil(k/S):
+//       S*J >= k distinct elements are at least that large),
+//   (b) the smallest of the warps' current J-th best values (again S*J >= k elements above it),
+//   (c) the warp's own k-th best,
+// and a batch is skipped with one vote when no lane's maximum reaches their maximum.  At the
+// end every warp keeps only its list entries at or above the final bounds, and one warp merges
+// them (rank counting on 64-bit keys) into the row's top-k.
+template <bool VEC>
+__global__ void __launch_bounds__(1024) row_topk_kernel(const float* __restrict__ logp, int V,
+                                                        int seg_len, int k,
+                                                        float* __restrict__ row_v,
+                                                        int* __restrict__ row_i) {
+  constexpr int U = 4;
+  __shared__ unsigned s_pro[32];
+  __shared__ float s_jth[32];
+  __shared__ float s_kth[32];
+  __shared__ unsigned long long s_surv[32 * TS_MAX_TOPK];
+  __shared__ unsigned long long s_scratch[TS_MAX_TOPK];
+  __shared__ int s_n;
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int S = blockDim.x >> 5;
+  const int J = (k + S - 1) / S;
+  const long long row = blockIdx.x;
   const float* x = logp + row * static_cast<long long>(V);
-  const int begin = seg * seg_len;
+  const int begin = warp * seg_len;
   const int end = min(V, begin + seg_len);
+  const int q0 = begin >> 2, q1 = (end + 3) >> 2;
+  if (lane == 0) s_jth[warp] = -INFINITY;
+  if (threadIdx.x == 0) s_n = 0;
   WarpTopk t;
   wtopk_init(t);
-  if (vec) {
-    constexpr int U = 8;
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    const int b4 = begin >> 2, e4 = end >> 2;
-    for (int i0 = b4; i0 < e4; i0 += U * 32) {
-      float4 a[U];
+  float4 nx[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * 32 + lane;
-        a[u] = i < e4 ? __ldcs(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int u = 0; u < U; ++u) nx[u] = load_quad<VEC>(x, q0 + u * 32 + lane, end);
+
+  // (a): every warp contributes its J largest lane maxima of the first batch
+  float t_pro;
+  {
+    float lm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u) lm = fmaxf(lm, fmaxf(fmaxf(nx[u].x, nx[u].y), fmaxf(nx[u].z, nx[u].w)));
+    warp_kth_key(lm == lm ? float_order_key(lm) : 0u, J, s_pro + warp * J, lane);
+    __syncthreads();
+    const unsigned kth = warp_kth_key(lane < S * J ? s_pro[lane] : 0u, k, nullptr, lane);
+    t_pro = kth == 0u ? -INFINITY : key_to_float(kth);
+  }
+
+  float pub = -INFINITY;  // this warp's J-th best as last published
+  for (int qb = q0; qb < q1; qb += U * 32) {
+    float4 a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      a[u] = nx[u];
+      nx[u] = load_quad<VEC>(x, qb + (U + u) * 32 + lane, end);
+    }
+    // (b): the smallest J-th best over the warps
+    float jm = lane < S ? *reinterpret_cast<volatile float*>(&s_jth[lane]) : INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) jm = fminf(jm, __shfl_xor_sync(0xffffffffu, jm, off));
+    const float lo = fmaxf(fmaxf(t_pro, jm), t.thr_v);
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u) bm = fmaxf(bm, fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w)));
+    if (__ballot_sync(0xffffffffu, bm >= lo) == 0u) continue;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = qb + u * 32 + lane;
+      const float mx = fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w));
+      const bool hot = 4 * q < end && mx >= lo;  // (the -inf padding past the end must not enter)
+      if (__ballot_sync(0xffffffffu, hot) == 0u) continue;
+      unsigned cm = 0u;
+      if (hot) {
+        const int left = end - 4 * q;  // elements of this quad inside the segment (>= 1)
+        cm = (a[u].x >= lo ? 1u : 0u) | (a[u].y >= lo && left > 1 ? 2u : 0u) |
+             (a[u].z >= lo && left > 2 ? 4u : 0u) | (a[u].w >= lo && left > 3 ? 8u : 0u);
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * 32 + lane;
-        const float mx = fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w));
-        const bool hot = i < e4 && mx >= t.thr_v;
-        if (__ballot_sync(0xffffffffu, hot) == 0u) continue;
-        // lanes without a candidate offer the sentinel (-inf, INT_MAX), which never enters
-        wtopk_offer(t, hot ? a[u].x : -INFINITY, hot ? (i << 2) : INT_MAX, k);
-        wtopk_offer(t, hot ? a[u].y : -INFINITY, hot ? (i << 2) + 1 : INT_MAX, k);
-        wtopk_offer(t, hot ? a[u].z : -INFINITY, hot ? (i << 2) + 2 : INT_MAX, k);
-        wtopk_offer(t, hot ? a[u].w : -INFINITY, hot ? (i << 2) + 3 : INT_MAX, k);
+      // one offer per candidate element (lanes without one offer the sentinel)
+      while (__ballot_sync(0xffffffffu, cm != 0u)) {
+        const int c = __ffs(cm) - 1;
+        const float xv = c == 0 ? a[u].x : c == 1 ? a[u].y : c == 2 ? a[u].z : a[u].w;
+        wtopk_offer(t, cm ? xv : -INFINITY, cm ? 4 * q + c : INT_MAX, k);
+        cm &= cm - 1u;
       }
     }
-  } else {
-    for (int i0 = begin; i0 < end; i0 += 32) {
-      const int i = i0 + lane;
-      wtopk_offer(t, i < end ? __ldcs(x + i) : -INFINITY, i < end ? i : INT_MAX, k);
+    const float jv = __shfl_sync(0xffffffffu, t.v, J - 1);
+    if (jv > pub) {
+      pub = jv;
+      if (lane == 0) s_jth[warp] = jv;
     }
   }
-  if (lane < k) {
-    const long long o = item * k + lane;
-    part_v[o] = t.v;
-    part_i[o] = t.i;
+
+  // final bounds; the surviving list entries of all warps go to one array
+  if (lane == 0) s_kth[warp] = t.thr_v;
+  __syncthreads();
+  {
+    float jm = lane < S ? s_jth[lane] : INFINITY;
+    float km = lane < S ? s_kth[lane] : -INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      jm = fminf(jm, __shfl_xor_sync(0xffffffffu, jm, off));
+      km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, off));
+    }
+    const float lof = fmaxf(t_pro, fmaxf(jm, km));
+    const bool keep = lane < k && t.i != INT_MAX && t.v >= lof;
+    const unsigned msk = __ballot_sync(0xffffffffu, keep);
+    int base = 0;
+    if (lane == 0 && msk != 0u) base = atomicAdd(&s_n, __popc(msk));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (keep) s_surv[base + __popc(msk & ((1u << lane) - 1u))] = cand_key(t.v, t.i);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = s_n;
+    unsigned long long lk = 0ull;
+    for (int c0 = 0; c0 < n; c0 += 32) lk = merge_keys(lk, s_surv + c0, min(32, n - c0), k, s_scratch, lane);
+    if (lane < k) {
+      float v = -INFINITY;
+      int idx = INT_MAX;
+      if (lk != 0ull) {
+        idx = static_cast<int>(0xffffffffu - static_cast<unsigned>(lk));
+        v = key_to_float(static_cast<unsigned>(lk >> 32));
+        if (v == 0.0f) v = x[idx];  // keep the sign of a zero
+      }
+      row_v[row * k + lane] = v;
+      row_i[row * k + lane] = idx;
+    }
   }
 }
 
@@ -141,12 +277,12 @@ __global__ void __launch_bounds__(kTopkThreads) row_topk_kernel(
 struct TreeSmem {
   int N;  // candidates
   int off_val, off_key, off_rtok, off_rlp, off_tok, off_lrank, off_sorted, off_flat, off_sel;
-  int off_cntc, off_cnt, off_par, off_err, off_stage, off_racc, total;
+  int off_cntc, off_cnt, off_par, off_err, off_racc, off_skey, off_pfs, total;
 };
 
 __host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
 
-__host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, int m, int S) {
+__host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, int m) {
   TreeSmem L;
   L.N = k + (depth - 1) * k * k;
   int o = 0;
@@ -164,7 +300,8 @@ __host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, in
   L.off_par = o;    o = align8(o + 4 * m);                // flat parent
   L.off_err = o;    o = align8(o + 4);
   L.off_racc = o;   o = align8(o + 4 * k * k);            // rank accumulators of one layer
-  L.off_stage = o;  o = align8(o + 8 * (kTreeThreads / 32) * S * k);  // per-warp partial lists
+  L.off_skey = o;   o = align8(o + 8 * L.N);              // per layer: keys in rank order
+  L.off_pfs = o;    o = align8(o + 4 * 2 * TS_MAX_TOPK);  // flat index of each frontier slot
   L.total = o;
   return L;
 }
@@ -193,7 +330,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     int32_t* __restrict__ tokens, int32_t* __restrict__ parents, int32_t* __restrict__ depth_out,
     uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const TreeSmem L = tree_smem_layout(k, depth, R, m, S);
+  pdl_launch_dependents();
+  pdl_wait();
+  const TreeSmem L = tree_smem_layout(k, depth, R, m);
   double* cV = reinterpret_cast<double*>(smem + L.off_val);
   unsigned long long* ckey = reinterpret_cast<unsigned long long*>(smem + L.off_key);
   int* rtok = reinterpret_cast<int*>(smem + L.off_rtok);
@@ -207,64 +346,19 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
   int* cnt = reinterpret_cast<int*>(smem + L.off_cnt);
   int* fpar = reinterpret_cast<int*>(smem + L.off_par);
   int* err = reinterpret_cast<int*>(smem + L.off_err);
+  unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + L.off_skey);
+  int* pfs = reinterpret_cast<int*>(smem + L.off_pfs);
 
   const int b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int nwarps = kTreeThreads / 32;
+  const int tid = threadIdx.x;
   const long long out0 = static_cast<long long>(b) * m;
 
   if (tid == 0) *err = 0;
   if (m > 1) {
-    // 1. Merge each row's S sorted segment lists (k each) into the row's top-k.  The
-    //    warp first copies the row's S*k partials to shared memory (independent loads).
-    float* wv = reinterpret_cast<float*>(smem + L.off_stage) + warp * S * k;
-    int* wi = reinterpret_cast<int*>(smem + L.off_stage + 4 * nwarps * S * k) + warp * S * k;
-    for (int r = warp; r < R; r += nwarps) {
-      const long long base = (static_cast<long long>(b) * R + r) * S * k;
-      for (int e0 = lane; e0 < S * k; e0 += 8 * 32) {  // 8 independent loads in flight
-        float v8[8];
-        int i8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = e0 + 32 * u;
-          if (e < S * k) {
-            v8[u] = part_v[base + e];
-            i8[u] = part_i[base + e];
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = e0 + 32 * u;
-          if (e < S * k) {
-            wv[e] = v8[u];
-            wi[e] = i8[u];
-          }
-        }
-      }
-      __syncwarp();
-      // k rounds: the best head among the S lists (largest value, then lowest id) is taken
-      // with two warp reductions on an order-preserving 32-bit key and the id.
-      int ptr = 0;
-      for (int j = 0; j < k; ++j) {
-        float v = -INFINITY;
-        int i = INT_MAX;
-        if (lane < S && ptr < k) {
-          v = wv[lane * k + ptr];
-          i = wi[lane * k + ptr];
-        }
-        const unsigned key = float_order_key(v);
-        const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
-        const int imin = __reduce_min_sync(0xffffffffu, key == kmax ? i : INT_MAX);
-        const bool win = key == kmax && i == imin;
-        const int wl = __ffs(__ballot_sync(0xffffffffu, win)) - 1;
-        const float best_v = __shfl_sync(0xffffffffu, v, wl < 0 ? 0 : wl);
-        if (lane < S && ptr < k && win) ++ptr;
-        if (lane == 0) {
-          rtok[r * k + j] = imin;
-          rlp[r * k + j] = best_v;
-        }
-      }
-      __syncwarp();
+    // 1. The rows' top-k lists (already merged by row_topk_kernel).
+    for (int e = tid; e < R * k; e += kTreeThreads) {
+      rlp[e] = part_v[static_cast<long long>(b) * R * k + e];
+      rtok[e] = part_i[static_cast<long long>(b) * R * k + e];
     }
     for (int x = tid; x < (depth + 1) * k; x += kTreeThreads) cntc[x] = 0;
     for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
@@ -302,6 +396,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         for (int t = tid; t < n; t += kTreeThreads) {
           lrank[t] = static_cast<short>(t);
           sorted[t] = static_cast<short>(t);
+          skey[t] = ckey[t];
         }
       } else {
         int* racc = reinterpret_cast<int*>(smem + L.off_racc);
@@ -322,6 +417,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           const int rank = racc[t];
           lrank[base + t] = static_cast<short>(rank);
           sorted[base + rank] = static_cast<short>(base + t);
+          skey[base + rank] = ckey[base + t];
         }
       }
       __syncthreads();
@@ -336,12 +432,12 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       int g = lrank[x];
       for (int l2 = 1; l2 <= depth; ++l2) {
         if (l2 == l) continue;
-        const int base2 = layer_base(l2, k), n2 = layer_size(l2, k);
+        const unsigned long long* keys2 = skey + layer_base(l2, k);  // that layer, in rank order
         const bool shallower = l2 < l;
-        int lo = 0, hi = n2;
+        int lo = 0, hi = layer_size(l2, k);
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
-          const unsigned long long kw = ckey[sorted[base2 + mid]];
+          const unsigned long long kw = keys2[mid];
           if (shallower ? (kw >= kv) : (kw > kv)) lo = mid + 1; else hi = mid;
         }
         g += lo;
@@ -381,16 +477,18 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
         const int j = (l == 1) ? 0 : t / k, c = t % k;
         int pos = 0, pf = 0;
         if (l > 1) {
-          const int pbase = layer_base(l - 1, k);
-          pf = cflat[sorted[pbase + j]];
+          const int* pf_prev = pfs + ((l - 1) & 1) * TS_MAX_TOPK;  // flat index per slot
+          pf = pf_prev[j];
           for (int j2 = 0; j2 < k; ++j2) {
-            if (j2 == j || cntc[l * k + j2] == 0) continue;
-            if (cflat[sorted[pbase + j2]] < pf) pos += cntc[l * k + j2];
+            const int cj = cntc[l * k + j2];
+            if (j2 != j && cj != 0 && pf_prev[j2] < pf) pos += cj;
           }
         }
         for (int c2 = 0; c2 < c; ++c2) pos += sel[base + j * k + c2];
         const int f = off + pos;
         cflat[x] = static_cast<short>(f);
+        const int rk = lrank[x];
+        if (rk < k) pfs[(l & 1) * TS_MAX_TOPK + rk] = f;  // x is frontier slot rk of layer l
         fpar[f] = pf;
         tokens[out0 + f] = ctok[x];
         parents[out0 + f] = pf;
@@ -432,19 +530,17 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
 
 }  // namespace
 
-// Segments per draft row (one warp each): at least 8 warps per SM when the rows allow it,
-// at most 32 (one per lane of the merging warp), segment length a multiple of 4 (16-byte
-// loads) and at least 1024 floats.
+// Warps per draft row (one CTA of S warps per row): as many as keep every row's CTA resident at
+// once (at most 1024 threads per SM at 64 registers a thread), at most 32, and segments of
+// about 1024 elements or more; the segment length is a multiple of 4 (16-byte loads).
 static void build_plan(int B, int V, int k, int depth, int num_sms, int* S_out, int* seg_out) {
   if (num_sms < 1) num_sms = 1;
   const int R = 1 + (depth - 1) * k;
   const long long rows = static_cast<long long>(B) * R;
-  int S = (V + 16383) / 16384;
-  const long long want = (8LL * num_sms + rows - 1) / rows;
-  if (want > S) S = static_cast<int>(want);
+  const long long per_sm = (rows + num_sms - 1) / num_sms;
+  int S = per_sm >= 32 ? 1 : static_cast<int>(32 / per_sm);
   const int max_by_len = (V + 1023) / 1024;
   if (S > max_by_len) S = max_by_len;
-  if (S > 32) S = 32;
   if (S < 1) S = 1;
   int seg = (V + S - 1) / S;
   seg = (seg + 3) & ~3;
@@ -457,7 +553,7 @@ size_t tree_build_workspace_bytes(int B, int V, int k, int depth, int num_sms) {
   int S, seg;
   build_plan(B, V, k, depth, num_sms, &S, &seg);
   const long long R = 1 + static_cast<long long>(depth - 1) * k;
-  return static_cast<size_t>(B) * R * S * k * 8 + 256;
+  return static_cast<size_t>(B) * R * k * 8 + 256;  // each row's merged top-k
 }
 
 int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
@@ -469,27 +565,30 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
   build_plan(B, V, k, depth, num_sms, &S, &seg);
   const long long rows = static_cast<long long>(B) * R;
   float* part_v = static_cast<float*>(workspace);
-  int* part_i = reinterpret_cast<int*>(part_v + rows * S * k);
+  int* part_i = reinterpret_cast<int*>(part_v + rows * k);
   const int W = (m + 63) / 64;
   int launches = 0;
   if (m > 1) {
-    const int vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(draft_logp) % 16 == 0);
-    const long long grid = (rows * S + kTopkThreads / 32 - 1) / (kTopkThreads / 32);
-    if (grid > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
-    row_topk_kernel<<<static_cast<unsigned>(grid), kTopkThreads, 0, stream>>>(draft_logp, V, seg, S, k,
-                                                                              vec, rows * S, part_v, part_i);
+    const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(draft_logp) % 16 == 0);
+    if (rows > 0x7fffffffLL) return TS_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(rows)), block(32 * S);
+    const cudaError_t e = vec ? launch_pdl(row_topk_kernel<true>, grid, block, 0, stream, draft_logp, V, seg, k,
+                                           part_v, part_i)
+                              : launch_pdl(row_topk_kernel<false>, grid, block, 0, stream, draft_logp, V, seg,
+                                           k, part_v, part_i);
+    if (e != cudaSuccess) return TS_ERR_CUDA;
     ++launches;
   }
-  const TreeSmem L = tree_smem_layout(k, depth, R, m, S);
+  const TreeSmem L = tree_smem_layout(k, depth, R, m);
   const int smem = L.total;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return TS_ERR_CUDA;
   }
-  tree_kernel<<<B, kTreeThreads, smem, stream>>>(part_v, part_i, root_tokens, R, S, k, depth, m,
-                                                  W, tokens, parents, depth_out, mask, values,
-                                                  dev_status);
+  if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), smem, stream, part_v, part_i, root_tokens, R, S, k,
+                 depth, m, W, tokens, parents, depth_out, mask, values, dev_status) != cudaSuccess)
+    return TS_ERR_CUDA;
   ++launches;
   count_launches(launches);
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;

@@ -79,6 +79,38 @@ def test_ties_everywhere():
     _run_and_compare(logp.contiguous(), torch.tensor([1, 2], dtype=torch.int32), k, depth, m)
 
 
+@pytest.mark.parametrize("order", ["ascending", "descending", "constant", "one_finite"])
+def test_row_orders_that_defeat_early_bounds(order):
+    """Row layouts chosen against the streaming top-k: every element a new best (ascending), no
+    candidate after the first batch (descending), ties everywhere (constant: the k smallest
+    indices win), and a single finite entry per row (the rest of each top-k is -inf, taken by
+    smallest index).  Rows long enough for several batches per warp."""
+    B, k, depth, m, V = 2, 6, 4, 30, 40000
+    R = 1 + (depth - 1) * k
+    ramp = torch.linspace(-20.0, -1.0, V)
+    if order == "ascending":
+        logp = ramp.expand(B, R, V)
+    elif order == "descending":
+        logp = ramp.flip(0).expand(B, R, V)
+    elif order == "constant":
+        logp = torch.full((B, R, V), -3.0)
+    else:
+        logp = torch.full((B, R, V), float("-inf"))
+        g = torch.Generator().manual_seed(5)
+        pos = torch.randint(0, V, (B, R), generator=g)
+        logp.scatter_(2, pos.unsqueeze(-1), -0.5)
+    _run_and_compare(logp.contiguous(), torch.tensor([3, 4], dtype=torch.int32), k, depth, m)
+
+
+def test_many_rows_one_warp_each():
+    """More draft rows than 32 per SM: one warp per row (the whole row in one segment)."""
+    B, k, depth, m, V = 64, 10, 8, 64, 3000
+    R = 1 + (depth - 1) * k
+    logp = _logp(B, R, V, seed=17)
+    roots = torch.arange(B, dtype=torch.int32) % V
+    _run_and_compare(logp, roots, k, depth, m)
+
+
 def test_unaligned_rows_take_the_scalar_path():
     B, k, depth, m, V = 2, 3, 4, 20, 1024
     R = 1 + (depth - 1) * k
