@@ -404,16 +404,20 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         const int key0 = (t0 + t) * BN;
         float mx = -INFINITY;
         if (key0 + BN > L) {
+          // one visibility bit per column: the prefix columns, then this row's ancestor bits of
+          // the tree positions the tile covers (positions at or past m are never visible)
+          const int pre = L - key0;             // prefix columns in this tile (< 64)
+          const int tt0 = pre > 0 ? 0 : -pre;   // first tree position in this tile
+          const int q = tt0 >> 6, sh = tt0 & 63;
+          const uint64_t lo = q == 0 ? mw0 : q == 1 ? mw1 : q == 2 ? mw2 : q == 3 ? mw3 : 0ull;
+          const uint64_t hi = q == 0 ? mw1 : q == 1 ? mw2 : q == 2 ? mw3 : 0ull;
+          uint64_t tb = sh == 0 ? lo : (lo >> sh) | (hi << (64 - sh));
+          const int ntree = p.m - tt0;          // tree positions left from tt0
+          if (ntree < 64) tb &= ntree > 0 ? (1ull << ntree) - 1ull : 0ull;
+          const uint64_t vis = pre > 0 ? (((1ull << pre) - 1ull) | (tb << pre)) : tb;
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
-            const int key = key0 + c;
-            bool vis = key < L;
-            if (!vis && key < nkeys) {
-              const int tt = key - L;
-              const uint64_t w = tt < 64 ? mw0 : tt < 128 ? mw1 : tt < 192 ? mw2 : mw3;
-              vis = (w >> (tt & 63)) & 1ull;
-            }
-            s[c] = vis ? s[c] : -INFINITY;
+            s[c] = ((vis >> c) & 1ull) ? s[c] : -INFINITY;
             mx = fmaxf(mx, s[c]);
           }
         } else {
