@@ -44,11 +44,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // ---------------------------------------------------------------------------------
 // programmatic dependent launch: every library kernel is launched with programmatic stream
 // serialization and waits for the previous grid (whatever it was) before it reads any input,
-// so its launch and CTA placement overlap the previous kernel's tail.  Only kernels whose grid
-// is a handful of CTAs (tree_kernel, accept_kernel) or whose dependent is one (the argmax
-// stream, followed by accept_kernel) let the next grid in at their start: CTAs of a dependent
-// grid that sit waiting next to a wide, still-running grid slowed it down measurably (a draft
-// row stream followed by tree_kernel took 7-26 us longer), so wide kernels trigger at exit.
+// so its launch and CTA placement overlap the previous kernel's tail.  A kernel lets the next
+// grid in early only where little of its own work is left (tree_kernel before its mask pass,
+// accept_kernel after its loads) or where its dependent is a handful of CTAs (the argmax stream,
+// followed by accept_kernel): CTAs of a dependent grid that sat waiting next to a still-running
+// kernel slowed it down measurably (a draft-row stream followed by tree_kernel took 7-26 us
+// longer), so the wide kernels trigger at exit.
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
   __shared__ int s_par[TS_MAX_NODES];
   __shared__ int s_tok[TS_MAX_NODES];
   __shared__ unsigned s_key[32];
-  pdl_launch_dependents();
   pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
   const long long r0 = static_cast<long long>(b) * m;
@@ -175,7 +174,9 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
     s_tok[i] = tokens[r0 + i];
     bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
   }
-  if (__syncthreads_or(bad)) {
+  const bool any_bad = __syncthreads_or(bad);
+  pdl_launch_dependents();  // only on-chip work is left
+  if (any_bad) {
     if (i == 0) {
       report(status, TS_ERR_DEVICE_CHECK);
       accept_len[b] = 0;

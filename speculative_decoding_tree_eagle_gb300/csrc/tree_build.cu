@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(1024) row_topk_kernel(const float* __restrict_
 // Shared-memory layout of tree_kernel (sizes depend on k, depth, R, m).
 struct TreeSmem {
   int N;  // candidates
-  int off_val, off_key, off_rtok, off_rlp, off_tok, off_lrank, off_sorted, off_flat, off_sel;
-  int off_cntc, off_cnt, off_par, off_err, off_racc, off_skey, off_pfs, total;
+  int off_val, off_key, off_code, off_skey, off_rtok, off_rlp, off_tok, off_lrank, off_sorted;
+  int off_cpar, off_flat, off_sel, off_cnt, off_par, off_err, total;
 };
 
 __host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
@@ -288,20 +288,19 @@ __host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, in
   int o = 0;
   L.off_val = o;    o = align8(o + 8 * L.N);              // fp64 value (sum of log-probs)
   L.off_key = o;    o = align8(o + 8 * L.N);              // order-preserving integer key
+  L.off_code = o;   o = align8(o + 8 * L.N);              // path code: child ranks in base k
+  L.off_skey = o;   o = align8(o + 8 * L.N);              // per layer: keys in rank order
   L.off_rtok = o;   o = align8(o + 4 * R * k);            // row top-k tokens
   L.off_rlp = o;    o = align8(o + 4 * R * k);            // row top-k log-probs
   L.off_tok = o;    o = align8(o + 4 * L.N);              // candidate token
   L.off_lrank = o;  o = align8(o + 2 * L.N);              // rank within its layer
   L.off_sorted = o; o = align8(o + 2 * L.N);              // per layer: ids by rank
+  L.off_cpar = o;   o = align8(o + 2 * L.N);              // parent candidate (-1 for layer 1)
   L.off_flat = o;   o = align8(o + 2 * L.N);              // flat index or -1
   L.off_sel = o;    o = align8(o + L.N);                  // selected flag
-  L.off_cntc = o;   o = align8(o + 4 * (depth + 1) * k);  // selected children per frontier slot
   L.off_cnt = o;    o = align8(o + 4 * (depth + 2));      // selected per layer
   L.off_par = o;    o = align8(o + 4 * m);                // flat parent
   L.off_err = o;    o = align8(o + 4);
-  L.off_racc = o;   o = align8(o + 4 * k * k);            // rank accumulators of one layer
-  L.off_skey = o;   o = align8(o + 8 * L.N);              // per layer: keys in rank order
-  L.off_pfs = o;    o = align8(o + 4 * 2 * TS_MAX_TOPK);  // flat index of each frontier slot
   L.total = o;
   return L;
 }
@@ -326,28 +325,27 @@ __device__ __forceinline__ unsigned long long order_key(double v) {
 
 __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     const float* __restrict__ part_v, const int* __restrict__ part_i,
-    const int32_t* __restrict__ root_tokens, int R, int S, int k, int depth, int m, int W,
+    const int32_t* __restrict__ root_tokens, int R, int k, int depth, int m, int W,
     int32_t* __restrict__ tokens, int32_t* __restrict__ parents, int32_t* __restrict__ depth_out,
     uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  pdl_launch_dependents();
   pdl_wait();
   const TreeSmem L = tree_smem_layout(k, depth, R, m);
   double* cV = reinterpret_cast<double*>(smem + L.off_val);
   unsigned long long* ckey = reinterpret_cast<unsigned long long*>(smem + L.off_key);
+  unsigned long long* ccode = reinterpret_cast<unsigned long long*>(smem + L.off_code);
+  unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + L.off_skey);
   int* rtok = reinterpret_cast<int*>(smem + L.off_rtok);
   float* rlp = reinterpret_cast<float*>(smem + L.off_rlp);
   int* ctok = reinterpret_cast<int*>(smem + L.off_tok);
   short* lrank = reinterpret_cast<short*>(smem + L.off_lrank);
   short* sorted = reinterpret_cast<short*>(smem + L.off_sorted);
+  short* cpar = reinterpret_cast<short*>(smem + L.off_cpar);
   short* cflat = reinterpret_cast<short*>(smem + L.off_flat);
   unsigned char* sel = smem + L.off_sel;
-  int* cntc = reinterpret_cast<int*>(smem + L.off_cntc);
   int* cnt = reinterpret_cast<int*>(smem + L.off_cnt);
   int* fpar = reinterpret_cast<int*>(smem + L.off_par);
   int* err = reinterpret_cast<int*>(smem + L.off_err);
-  unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + L.off_skey);
-  int* pfs = reinterpret_cast<int*>(smem + L.off_pfs);
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -355,43 +353,46 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
 
   if (tid == 0) *err = 0;
   if (m > 1) {
-    // 1. The rows' top-k lists (already merged by row_topk_kernel).
+    // 1. The rows' top-k lists (row_topk_kernel's output).
     for (int e = tid; e < R * k; e += kTreeThreads) {
       rlp[e] = part_v[static_cast<long long>(b) * R * k + e];
       rtok[e] = part_i[static_cast<long long>(b) * R * k + e];
     }
-    for (int x = tid; x < (depth + 1) * k; x += kTreeThreads) cntc[x] = 0;
     for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
     __syncthreads();
 
     // 2. Expansion, layer by layer: value = parent value + log-prob (fp64, root -> leaf);
-    //    frontier slot j of layer l-1 is the candidate of rank j in that layer.
+    //    frontier slot j of layer l-1 is the candidate of rank j in that layer.  A candidate's
+    //    path code is its parent's code times k plus its child rank.
     for (int l = 1; l <= depth; ++l) {
       const int base = layer_base(l, k), n = layer_size(l, k);
       for (int t = tid; t < n; t += kTreeThreads) {
         double v;
-        int tok;
+        int tok, par;
+        unsigned long long code;
         if (l == 1) {
           tok = rtok[t];
           v = 0.0 + static_cast<double>(rlp[t]);
+          par = -1;
+          code = static_cast<unsigned long long>(t);
         } else {
-          const int j = t / k, c = t % k;
-          const int par = sorted[layer_base(l - 1, k) + j];
+          const int j = t / k, c = t - j * k;
+          par = sorted[layer_base(l - 1, k) + j];
           const int row = 1 + (l - 2) * k + j;
           tok = rtok[row * k + c];
           v = cV[par] + static_cast<double>(rlp[row * k + c]);
+          code = ccode[par] * static_cast<unsigned long long>(k) + static_cast<unsigned long long>(c);
         }
         ctok[base + t] = tok;
         cV[base + t] = v;
         ckey[base + t] = order_key(v);
-        if (l > 1) reinterpret_cast<int*>(smem + L.off_racc)[t] = t % k;
+        ccode[base + t] = code;
+        cpar[base + t] = static_cast<short>(par);
       }
       __syncthreads();
-      // rank inside the layer (value descending, ties -> lower layer-local index).  Layer 1
-      // is the root row's top-k, already in order.  A later layer is k sorted lists (the k
-      // children of each frontier slot, in child-rank order): the rank of child c of slot j
-      // is c plus, for every other slot, the number of its children that come first, found
-      // by a binary search; one thread per (candidate, other slot) pair.
+      // rank inside the layer: value descending, ties -> lower layer-local index.  Layer 1 is
+      // the root row's top-k, already in that order.  Otherwise P threads per candidate count
+      // the candidates that come first, each over every P-th candidate, and add up by shuffles.
       if (l == 1) {
         for (int t = tid; t < n; t += kTreeThreads) {
           lrank[t] = static_cast<short>(t);
@@ -399,40 +400,51 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           skey[t] = ckey[t];
         }
       } else {
-        int* racc = reinterpret_cast<int*>(smem + L.off_racc);
-        for (int q = tid; q < n * k; q += kTreeThreads) {
-          const int t = q / k, j2 = q % k, j = t / k;
-          if (j2 == j) continue;
-          const unsigned long long kv = ckey[base + t];
-          int lo = 0, hi = k;  // children of slot j2 that come before candidate t
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const unsigned long long kw = ckey[base + j2 * k + mid];
-            if (j2 < j ? (kw >= kv) : (kw > kv)) lo = mid + 1; else hi = mid;
+        int P = 1;
+        while (P < 32 && 2 * P * n <= kTreeThreads) P *= 2;
+        for (int q0 = 0; q0 < n * P; q0 += kTreeThreads) {
+          const int q = q0 + tid;
+          const int t = q / P, part = q & (P - 1);
+          const bool live = t < n;
+          const unsigned long long kv = live ? ckey[base + t] : 0ull;
+          int before = 0;
+          if (live) {
+            // eight independent loads in flight per step
+            int u = part;
+            for (; u + 7 * P < n; u += 8 * P) {
+              unsigned long long kw[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) kw[e] = ckey[base + u + e * P];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) before += (kw[e] > kv) | ((kw[e] == kv) & (u + e * P < t));
+            }
+            for (; u < n; u += P) {
+              const unsigned long long kw = ckey[base + u];
+              before += (kw > kv) | ((kw == kv) & (u < t));
+            }
           }
-          if (lo) atomicAdd(&racc[t], lo);
-        }
-        __syncthreads();
-        for (int t = tid; t < n; t += kTreeThreads) {
-          const int rank = racc[t];
-          lrank[base + t] = static_cast<short>(rank);
-          sorted[base + rank] = static_cast<short>(base + t);
-          skey[base + rank] = ckey[base + t];
+          for (int off = P >> 1; off > 0; off >>= 1) before += __shfl_xor_sync(0xffffffffu, before, off);
+          if (live && part == 0) {
+            lrank[base + t] = static_cast<short>(before);
+            sorted[base + before] = static_cast<short>(base + t);
+            skey[base + before] = kv;
+          }
         }
       }
       __syncthreads();
     }
 
     // 3. Rerank: global rank = rank in own layer + for every other layer the number of
-    //    its candidates that come first (higher value, or equal value and shallower),
-    //    found by binary search in that layer's sorted order.
+    //    its candidates that come first (higher value, or equal value and shallower), found
+    //    by binary search in that layer's sorted keys; a candidate stops counting once its
+    //    rank rules it out.
     for (int x = tid; x < L.N; x += kTreeThreads) {
       const int l = layer_of(x, k, depth);
       const unsigned long long kv = ckey[x];
       int g = lrank[x];
-      for (int l2 = 1; l2 <= depth; ++l2) {
+      for (int l2 = 1; l2 <= depth && g < m - 1; ++l2) {
         if (l2 == l) continue;
-        const unsigned long long* keys2 = skey + layer_base(l2, k);  // that layer, in rank order
+        const unsigned long long* keys2 = skey + layer_base(l2, k);
         const bool shallower = l2 < l;
         int lo = 0, hi = layer_size(l2, k);
         while (lo < hi) {
@@ -445,19 +457,12 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       const bool s = g < m - 1;
       sel[x] = s ? 1 : 0;
       cflat[x] = -1;
-      if (s) {
-        atomicAdd(&cnt[l], 1);
-        const int slot = (l == 1) ? 0 : (x - layer_base(l, k)) / k;
-        atomicAdd(&cntc[l * k + slot], 1);
-      }
+      if (s) atomicAdd(&cnt[l], 1);
     }
     __syncthreads();
     // connectivity: every selected node's parent must be selected
     for (int x = tid; x < L.N; x += kTreeThreads) {
-      if (!sel[x] || x < k) continue;
-      const int l = layer_of(x, k, depth);
-      const int j = (x - layer_base(l, k)) / k;
-      if (!sel[sorted[layer_base(l - 1, k) + j]]) *err = 1;
+      if (sel[x] && x >= k && !sel[cpar[x]]) *err = 1;
     }
     __syncthreads();
     if (*err) {
@@ -465,38 +470,41 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       return;
     }
 
-    // 4. Flatten: root, then by (depth, parent's flat index, child rank).  A node's
-    //    position in its depth = selected children of parents placed before its parent
-    //    + selected siblings of lower rank.
-    int off = 1;
-    for (int l = 1; l <= depth; ++l) {
+    // 4. Flatten: root, then by depth, and inside a depth by (parent's flat index, child
+    //    rank), which is the order of the path codes.  A node's flat index = 1 + the selected
+    //    nodes of shallower depths + the selected nodes of its depth with a smaller code.
+    for (int x = tid; x < L.N; x += kTreeThreads) {
+      if (!sel[x]) continue;
+      const int l = layer_of(x, k, depth);
+      int f = 1;
+      for (int l2 = 1; l2 < l; ++l2) f += cnt[l2];
       const int base = layer_base(l, k), n = layer_size(l, k);
-      for (int t = tid; t < n; t += kTreeThreads) {
-        const int x = base + t;
-        if (!sel[x]) continue;
-        const int j = (l == 1) ? 0 : t / k, c = t % k;
-        int pos = 0, pf = 0;
-        if (l > 1) {
-          const int* pf_prev = pfs + ((l - 1) & 1) * TS_MAX_TOPK;  // flat index per slot
-          pf = pf_prev[j];
-          for (int j2 = 0; j2 < k; ++j2) {
-            const int cj = cntc[l * k + j2];
-            if (j2 != j && cj != 0 && pf_prev[j2] < pf) pos += cj;
-          }
+      const unsigned long long code = ccode[x];
+      int y = base;
+      for (; y + 8 <= base + n; y += 8) {
+        unsigned long long cy[8];
+        unsigned char sy[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cy[e] = ccode[y + e];
+          sy[e] = sel[y + e];
         }
-        for (int c2 = 0; c2 < c; ++c2) pos += sel[base + j * k + c2];
-        const int f = off + pos;
-        cflat[x] = static_cast<short>(f);
-        const int rk = lrank[x];
-        if (rk < k) pfs[(l & 1) * TS_MAX_TOPK + rk] = f;  // x is frontier slot rk of layer l
-        fpar[f] = pf;
-        tokens[out0 + f] = ctok[x];
-        parents[out0 + f] = pf;
-        depth_out[out0 + f] = l;
-        if (values) values[out0 + f] = cV[x];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f += (sy[e] != 0) & (cy[e] < code);
       }
-      off += cnt[l];
-      __syncthreads();
+      for (; y < base + n; ++y) f += (sel[y] != 0) & (ccode[y] < code);
+      cflat[x] = static_cast<short>(f);
+    }
+    __syncthreads();
+    for (int x = tid; x < L.N; x += kTreeThreads) {
+      if (!sel[x]) continue;
+      const int f = cflat[x];
+      const int pf = x < k ? 0 : cflat[cpar[x]];
+      fpar[f] = pf;
+      tokens[out0 + f] = ctok[x];
+      parents[out0 + f] = pf;
+      depth_out[out0 + f] = layer_of(x, k, depth);
+      if (values) values[out0 + f] = cV[x];
     }
   }
   if (tid == 0) {
@@ -507,6 +515,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     if (values) values[out0] = 0.0;
   }
   __syncthreads();
+  // the next kernel's CTAs may be placed now: only the short mask pass is left
+  pdl_launch_dependents();
   // 5. Mask rows: walk the parent pointers from each node to the root.
   for (int i = tid; i < m; i += kTreeThreads) {
     uint64_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
@@ -586,7 +596,7 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
         cudaSuccess)
       return TS_ERR_CUDA;
   }
-  if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), smem, stream, part_v, part_i, root_tokens, R, S, k,
+  if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), smem, stream, part_v, part_i, root_tokens, R, k,
                  depth, m, W, tokens, parents, depth_out, mask, values, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   ++launches;
