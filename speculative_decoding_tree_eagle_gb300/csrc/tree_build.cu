@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(1024) row_topk_kernel(const float* __restrict_
 struct TreeSmem {
   int N;  // candidates
   int off_val, off_key, off_code, off_skey, off_rtok, off_rlp, off_tok, off_lrank, off_sorted;
-  int off_cpar, off_flat, off_sel, off_cnt, off_par, off_err, total;
+  int off_cpar, off_flat, off_sel, off_cnt, off_par, off_err, off_slist, total;
 };
 
 __host__ __device__ inline int align8(int x) { return (x + 7) & ~7; }
@@ -301,6 +301,7 @@ __host__ __device__ inline TreeSmem tree_smem_layout(int k, int depth, int R, in
   L.off_cnt = o;    o = align8(o + 4 * (depth + 2));      // selected per layer
   L.off_par = o;    o = align8(o + 4 * m);                // flat parent
   L.off_err = o;    o = align8(o + 4);
+  L.off_slist = o;  o = align8(o + 2 * (depth + 1) * m);  // per depth: its selected candidates
   L.total = o;
   return L;
 }
@@ -318,8 +319,8 @@ __device__ __forceinline__ int layer_of(int x, int k, int depth) {
 // Monotone map of a double to an unsigned key (larger value -> larger key).  -0 and +0 get
 // the same key, so integer comparisons order values exactly as fp64 comparisons do.
 __device__ __forceinline__ unsigned long long order_key(double v) {
-  if (v == 0.0) v = 0.0;
-  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  if ((b << 1) == 0ull) b = 0ull;  // -0 -> +0 (integer test: no fp64 compare)
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
   int* cnt = reinterpret_cast<int*>(smem + L.off_cnt);
   int* fpar = reinterpret_cast<int*>(smem + L.off_par);
   int* err = reinterpret_cast<int*>(smem + L.off_err);
+  short* slist = reinterpret_cast<short*>(smem + L.off_slist);
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -383,16 +385,20 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           v = cV[par] + static_cast<double>(rlp[row * k + c]);
           code = ccode[par] * static_cast<unsigned long long>(k) + static_cast<unsigned long long>(c);
         }
+        const unsigned long long key = order_key(v);
         ctok[base + t] = tok;
         cV[base + t] = v;
-        ckey[base + t] = order_key(v);
+        ckey[base + t] = key;
         ccode[base + t] = code;
         cpar[base + t] = static_cast<short>(par);
       }
       __syncthreads();
       // rank inside the layer: value descending, ties -> lower layer-local index.  Layer 1 is
       // the root row's top-k, already in that order.  Otherwise P threads per candidate count
-      // the candidates that come first, each over every P-th candidate, and add up by shuffles.
+      // the candidates that come first, each over every P-th candidate (eight independent
+      // shared loads in flight), and add up by shuffles.  (Counting with broadcast loads beat
+      // per-slot searches over the sorted runs here: the layer is small and the searches'
+      // dependent steps cost more than the extra comparisons.)
       if (l == 1) {
         for (int t = tid; t < n; t += kTreeThreads) {
           lrank[t] = static_cast<short>(t);
@@ -409,7 +415,6 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
           const unsigned long long kv = live ? ckey[base + t] : 0ull;
           int before = 0;
           if (live) {
-            // eight independent loads in flight per step
             int u = part;
             for (; u + 7 * P < n; u += 8 * P) {
               unsigned long long kw[8];
@@ -457,7 +462,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       const bool s = g < m - 1;
       sel[x] = s ? 1 : 0;
       cflat[x] = -1;
-      if (s) atomicAdd(&cnt[l], 1);
+      if (s) slist[l * m + atomicAdd(&cnt[l], 1)] = static_cast<short>(x);
     }
     __syncthreads();
     // connectivity: every selected node's parent must be selected
@@ -473,26 +478,24 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     // 4. Flatten: root, then by depth, and inside a depth by (parent's flat index, child
     //    rank), which is the order of the path codes.  A node's flat index = 1 + the selected
     //    nodes of shallower depths + the selected nodes of its depth with a smaller code.
-    for (int x = tid; x < L.N; x += kTreeThreads) {
-      if (!sel[x]) continue;
-      const int l = layer_of(x, k, depth);
+    for (int e = tid; e < depth * m; e += kTreeThreads) {
+      const int l = 1 + e / m, pos = e - (l - 1) * m;
+      const int nl = cnt[l];
+      if (pos >= nl) continue;
+      const int x = slist[l * m + pos];
       int f = 1;
       for (int l2 = 1; l2 < l; ++l2) f += cnt[l2];
-      const int base = layer_base(l, k), n = layer_size(l, k);
       const unsigned long long code = ccode[x];
-      int y = base;
-      for (; y + 8 <= base + n; y += 8) {
-        unsigned long long cy[8];
-        unsigned char sy[8];
+      const short* sl = slist + l * m;
+      int q = 0;
+      for (; q + 8 <= nl; q += 8) {
+        short ids[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          cy[e] = ccode[y + e];
-          sy[e] = sel[y + e];
-        }
+        for (int e2 = 0; e2 < 8; ++e2) ids[e2] = sl[q + e2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f += (sy[e] != 0) & (cy[e] < code);
+        for (int e2 = 0; e2 < 8; ++e2) f += ccode[ids[e2]] < code ? 1 : 0;
       }
-      for (; y < base + n; ++y) f += (sel[y] != 0) & (ccode[y] < code);
+      for (; q < nl; ++q) f += ccode[sl[q]] < code ? 1 : 0;
       cflat[x] = static_cast<short>(f);
     }
     __syncthreads();
