@@ -9,6 +9,8 @@ Plain, slow, obviously-correct numpy restatements of what the pages define:
   ("rainlin.net/posts/eagle", section 四 Tree Attention; "lesty.tech", sections 5 and 8).
 * :mod:`oracle.tree_accept`  — greedy acceptance of the longest matching root path
   ("lesty.tech", section 4; "rainlin.net/posts/eagle", sections 3.2 and 四).
+* :mod:`oracle.kv_commit`    — keep the accepted path's K/V rows and release the rejected
+  scratch pages ("lesty.tech", section 8).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
@@ -21,3 +23,4 @@ Parity status of each function is stated in its module header.
 from .tree_build import row_topk, tree_build, ancestor_mask, mask_to_words, words_to_mask  # noqa: F401
 from .tree_attention import tree_attention  # noqa: F401
 from .tree_accept import target_argmax, accept_longest_path  # noqa: F401
+from .kv_commit import kv_commit  # noqa: F401
