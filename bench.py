@@ -344,9 +344,63 @@ def run_ours(args, rank, world, dev):
                      "achieved": round(achieved_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved_gbs / peak, 4), "traffic": traffic},
     }
+    res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(step, w, ab, args, dev, world)
     return res, w, inp
+
+
+def run_kv_commit(step, w, args, flush, stream, world):
+    """The KV commit of the step's accepted paths (the row after the hot path): K calls on
+    the step's own accept outputs, block table and prefix lengths restored before each call
+    (outside the events), L2 flushed."""
+    ts = step.ts
+    d = step.d
+    table0 = d["block_table"].clone()
+    plen0 = d["prefix_len"].clone()
+    out = dict(freed_blocks=torch.empty_like(table0), freed_count=torch.empty_like(plen0))
+    alen = step.acc["accept_len"].clone()
+    apath = step.acc["accept_path"].clone()
+    times = []
+    for i in range(args.warmup + args.steps):
+        d["block_table"].copy_(table0)
+        d["prefix_len"].copy_(plen0)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ts.kv_commit(d["k_cache"], d["v_cache"], d["block_table"], d["prefix_len"], apath, alen, out=out,
+                     status=step.status)
+        b.record(stream)
+        if i >= args.warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    ts.check_status(step.status)
+    d["block_table"].copy_(table0)
+    d["prefix_len"].copy_(plen0)
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    al = alen.cpu().tolist()
+    pl = apath.cpu().tolist()
+    moved = sum(sum(1 for j in range(n) if pl[bb][j] != j) for bb, n in enumerate(al))
+    row = w.Hkv * w.d * (2 if w.dtype == "bf16" else 4)
+    max_blocks = int(table0.shape[1])
+    byts = moved * row * 2 * 2 + w.B * (max_blocks * 4 * 3 + w.m * 4 + 12)
+    res = {"ms": round(ms, 5), "accepted_rows": int(sum(al)), "moved_rows": int(moved),
+           "algorithmic_bytes": int(byts), "bound": "latency (a few rows per sequence; one CTA each)"}
+    cache_bytes = d["k_cache"].numel() * d["k_cache"].element_size() * 2
+    if not args.no_cpu_baseline and world == 1 and cache_bytes <= (256 << 20):
+        # the oracle beside it (cpu-baseline leg): same caches, table, lengths and paths
+        import oracle
+        view = (lambda t: t.cpu().view(torch.int16).numpy()) if w.dtype == "bf16" else (lambda t: t.cpu().numpy())
+        kh, vh = view(d["k_cache"]), view(d["v_cache"])
+        th, lh, ph, ah = table0.cpu().numpy(), plen0.cpu().numpy(), apath.cpu().numpy(), alen.cpu().numpy()
+        t0 = time.perf_counter()
+        reps = 0
+        while reps < 3 or time.perf_counter() - t0 < 1.0:
+            oracle.kv_commit(kh, vh, th, lh, ph, ah, w.m, workloads.BLOCK_SIZE)
+            reps += 1
+        res["oracle_ms"] = round((time.perf_counter() - t0) / reps * 1e3, 3)
+        res["oracle_note"] = "fp64 numpy oracle on the host (copies the whole cache per call), same inputs"
+    return res
 
 
 def run_e2e(step, w, ab, args, dev, world):

@@ -202,6 +202,43 @@ int ts_tree_accept_noalloc(const void* logits, ts_dtype dt, const int32_t* token
                            int32_t* argmax, int32_t* accept_len, int32_t* accept_path,
                            int32_t* bonus, int32_t* dev_status, void* stream);
 
+/*
+ * ts_kv_commit — after ts_tree_accept, keep the accepted path's K/V rows in the paged cache
+ * and release the scratch pages that held only rejected tree nodes.
+ *
+ * Source: "lesty.tech — EAGLE-2 vs. Medusa", section 8 (speculative rollback: the tree's K/V
+ * are written into reserved scratch pages during the verify pass; only the accepted path
+ * survives, the block table commits it and the rejected pages return to the free pool).
+ * With multi-token pages the page's "update the pointers only" holds for whole pages; the
+ * accepted rows inside the tree's pages are compacted first.
+ *
+ * Tree node i of sequence b sits at logical position prefix_len[b] + i (the layout
+ * ts_tree_attention reads).  For every sequence, with L = prefix_len[b], a = accept_len[b]:
+ *   - the K and V rows of node accept_path[b][j] move to logical position L + j, for every
+ *     KV head and j = 0..a-1 (every row is read before it can be overwritten);
+ *   - prefix_len[b] becomes L + a;
+ *   - the block-table entries of logical pages ceil((L+a)/bs) .. ceil((L+m)/bs)-1 are listed,
+ *     in that order, in freed_blocks[b][0..] (the rest of the row is -1; freed_count[b] of
+ *     them) and set to -1 in the block table.
+ *
+ * k_cache, v_cache   [num_blocks, Hkv, block_size, d] of dt (TS_F32 or TS_BF16), device, in/out.
+ * block_table        [B, max_blocks] int32, device, in/out.
+ * prefix_len         [B] int32, device, in/out.
+ * accept_path        [B, m] int32, device (ts_tree_accept's output; -1 padded).
+ * accept_len         [B] int32, device (1..m).
+ * freed_blocks       [B, max_blocks] int32, device, out.   freed_count [B] int32, device, out.
+ * All pointers are caller-owned device memory; nothing is allocated; one launch on `stream`.
+ * Errors: TS_ERR_INVALID (null pointer, non-positive size, d * element size not a multiple
+ * of 4) and TS_ERR_UNSUPPORTED (m > TS_MAX_NODES) before any launch.  A sequence whose
+ * prefix length is negative, whose accept length is outside 1..m, whose path does not start
+ * at the root or does not increase, whose pages do not fit max_blocks or whose touched page
+ * ids are out of range is left untouched and *dev_status is set to TS_ERR_DEVICE_CHECK.
+ */
+int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
+                 int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
+                 const int32_t* accept_path, const int32_t* accept_len, int B, int m,
+                 int32_t* freed_blocks, int32_t* freed_count, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "TreeSpecError", "library", "library_path", "launch_count", "status_string",
-    "tree_build", "tree_attention", "tree_accept", "new_status", "check_status",
+    "tree_build", "tree_attention", "tree_accept", "kv_commit", "new_status", "check_status",
     "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace", "tree_attention_plan",
 ]
 
@@ -69,6 +69,8 @@ def library():
         L.ts_tree_accept_workspace.argtypes = [I, I, I, I]
         L.ts_tree_accept.restype = I
         L.ts_tree_accept.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, S, P, P]
+        L.ts_kv_commit.restype = I
+        L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L
     return _lib
 
@@ -253,4 +255,31 @@ def tree_accept(logits: torch.Tensor, tokens: torch.Tensor, parents: torch.Tenso
     _check(L.ts_tree_accept(_p(logits), dt, _p(tokens), _p(parents), B, m, V, _p(out["argmax"]),
                             _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws),
                             ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+              prefix_len: torch.Tensor, accept_path: torch.Tensor, accept_len: torch.Tensor, *,
+              out: Optional[Dict[str, torch.Tensor]] = None,
+              status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """Keep the accepted path's K/V rows and release the rejected scratch pages, in place on
+    k_cache/v_cache [num_blocks,Hkv,bs,d], block_table [B,max_blocks] and prefix_len [B];
+    returns freed_blocks [B,max_blocks] (-1 padded) and freed_count [B]."""
+    L = library()
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("prefix_len", prefix_len, torch.int32)
+    _need_cuda("accept_path", accept_path, torch.int32)
+    _need_cuda("accept_len", accept_len, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, max_blocks = block_table.shape
+    m = accept_path.shape[1]
+    dev = k_cache.device
+    if out is None:
+        out = dict(freed_blocks=torch.empty(B, max_blocks, dtype=torch.int32, device=dev),
+                   freed_count=torch.empty(B, dtype=torch.int32, device=dev))
+    _check(L.ts_kv_commit(_p(k_cache), _p(v_cache), _dt(k_cache), nb, bs, hkv, d, _p(block_table), max_blocks,
+                          _p(prefix_len), _p(accept_path), _p(accept_len), B, m, _p(out["freed_blocks"]),
+                          _p(out["freed_count"]), _p(status), _stream()))
     return out

@@ -169,4 +169,21 @@ int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
                                 static_cast<cudaStream_t>(stream), sms);
 }
 
+int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
+                 int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
+                 const int32_t* accept_path, const int32_t* accept_len, int B, int m,
+                 int32_t* freed_blocks, int32_t* freed_count, int32_t* dev_status, void* stream) {
+  if (B <= 0 || m <= 0 || num_blocks <= 0 || block_size <= 0 || Hkv <= 0 || d <= 0 || max_blocks <= 0)
+    return TS_ERR_INVALID;
+  if (dt != TS_F32 && dt != TS_BF16) return TS_ERR_INVALID;
+  if ((d * (dt == TS_BF16 ? 2 : 4)) % 4 != 0) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES || B > 65535) return TS_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache || !block_table || !prefix_len || !accept_path || !accept_len ||
+      !freed_blocks || !freed_count)
+    return TS_ERR_INVALID;
+  return ts::kv_commit_launch(k_cache, v_cache, dt, num_blocks, block_size, Hkv, d, block_table,
+                              max_blocks, prefix_len, accept_path, accept_len, B, m, freed_blocks,
+                              freed_count, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

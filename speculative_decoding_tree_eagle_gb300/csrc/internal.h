@@ -52,4 +52,10 @@ int attention_tc_launch(const AttnArgs& a, int num_sms);
 void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4);
 int attention_simt_launch(const AttnArgs& a);
 
+int kv_commit_launch(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
+                     int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
+                     const int32_t* accept_path, const int32_t* accept_len, int B, int m,
+                     int32_t* freed_blocks, int32_t* freed_count, int32_t* dev_status,
+                     cudaStream_t stream);
+
 }  // namespace ts

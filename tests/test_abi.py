@@ -29,7 +29,7 @@ def declared_symbols():
 
 def test_header_declares_the_three_operations():
     syms = declared_symbols()
-    for s in ("ts_tree_build", "ts_tree_attention", "ts_tree_accept"):
+    for s in ("ts_tree_build", "ts_tree_attention", "ts_tree_accept", "ts_kv_commit"):
         assert s in syms
 
 
@@ -91,6 +91,22 @@ def test_tree_accept_validation(lib):
     assert _accept(lib, dt=3) == TS_ERR_INVALID
     assert _accept(lib, m=257) == TS_ERR_UNSUPPORTED
     assert _accept(lib, ptr=None) == TS_ERR_INVALID
+
+
+def _commit(lib, dt=1, nb=10, bs=16, hkv=2, d=128, maxb=4, B=1, m=8, ptr=1):
+    P = ptr
+    return lib.ts_kv_commit(P, P, dt, nb, bs, hkv, d, P, maxb, P, P, P, B, m, P, P, None, None)
+
+
+def test_kv_commit_validation(lib):
+    assert _commit(lib, B=0) == TS_ERR_INVALID
+    assert _commit(lib, m=0) == TS_ERR_INVALID
+    assert _commit(lib, bs=0) == TS_ERR_INVALID
+    assert _commit(lib, maxb=0) == TS_ERR_INVALID
+    assert _commit(lib, dt=3) == TS_ERR_INVALID
+    assert _commit(lib, d=3) == TS_ERR_INVALID          # bf16 rows of 6 bytes
+    assert _commit(lib, m=257) == TS_ERR_UNSUPPORTED
+    assert _commit(lib, ptr=None) == TS_ERR_INVALID
 
 
 def test_workspace_queries_are_positive_for_valid_sizes(lib):
