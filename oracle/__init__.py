@@ -11,6 +11,8 @@ Plain, slow, obviously-correct numpy restatements of what the pages define:
   ("lesty.tech", section 4; "rainlin.net/posts/eagle", sections 3.2 and 四).
 * :mod:`oracle.kv_commit`    — keep the accepted path's K/V rows and release the rejected
   scratch pages ("lesty.tech", section 8).
+* :mod:`oracle.lm_head`      — the target LM head's per-row argmax ("jialefu.github.io —
+  EAGLE-4 efficient LM head", local Top-k section; "lesty.tech", section 4).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
@@ -24,3 +26,4 @@ from .tree_build import row_topk, tree_build, ancestor_mask, mask_to_words, word
 from .tree_attention import tree_attention  # noqa: F401
 from .tree_accept import target_argmax, accept_longest_path  # noqa: F401
 from .kv_commit import kv_commit  # noqa: F401
+from .lm_head import lm_head_logits, lm_head_argmax, fp32_error_bound  # noqa: F401
