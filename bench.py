@@ -344,10 +344,62 @@ def run_ours(args, rank, world, dev):
                      "achieved": round(achieved_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved_gbs / peak, 4), "traffic": traffic},
     }
-    res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world)}
+    res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world),
+                        "lm_head_argmax": run_lm_head(w, args, flush, stream, dev)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(step, w, ab, args, dev, world)
     return res, w, inp
+
+
+# hidden size of the target model each workload is shaped after (the LM head is [V, d_model])
+D_MODEL = {"llama2_7b": 4096, "llama3_8b_gqa": 4096, "llama2_70b_gqa": 8192}
+
+
+def run_lm_head(w, args, flush, stream, dev):
+    """The target LM head with the per-row argmax fused into its GEMM (the row after the hot
+    path): hidden [B*m, d_model] x weight [V, d_model]^T, seeded Gaussian bf16 weights, K calls,
+    L2 flushed before each."""
+    import speculative_decoding_tree_eagle_gb300 as ts
+    K = D_MODEL.get(w.name.split("_prefix")[0], 4096)
+    M, V = w.B * w.m, w.V
+    g = torch.Generator(device=dev).manual_seed(20260 + 99)
+    hidden = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    weight = (torch.randn(V, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    out = dict(argmax=torch.empty(M, dtype=torch.int32, device=dev),
+               max_logit=torch.empty(M, dtype=torch.float32, device=dev))
+    ws = torch.empty(max(256, ts.library().ts_lm_head_argmax_workspace(M, V, K)), dtype=torch.uint8, device=dev)
+    status = ts.new_status(dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ts.lm_head_argmax(hidden, weight, out=out, workspace=ws, status=status)
+        b.record(stream)
+        if i >= args.warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    ts.check_status(status)
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    byts = (V * K + M * K) * 2 + M * 8
+    flops = 2.0 * M * V * K
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except Exception:
+        pass
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tf = peaks.get("bf16_tflops", 1900.0)
+    tb_s = byts / (ms * 1e-3) / 1e12
+    tflops = flops / (ms * 1e-3) / 1e12
+    t_hbm, t_tc = byts / (hbm * 1e9), flops / (tf * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    frac = (tb_s * 1e3 / hbm) if bound == "hbm" else (tflops / tf)
+    del hidden, weight
+    return {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": K}, "algorithmic_bytes": int(byts),
+            "tb_s": round(tb_s, 4), "tflops": round(tflops, 2), "bound": bound, "frac_of_measured_peak": round(frac, 4),
+            "logits_bytes_not_written": int(M * V * 4)}
 
 
 def run_kv_commit(step, w, args, flush, stream, world):

@@ -202,6 +202,44 @@ int ts_tree_accept_noalloc(const void* logits, ts_dtype dt, const int32_t* token
                            int32_t* argmax, int32_t* accept_len, int32_t* accept_path,
                            int32_t* bonus, int32_t* dev_status, void* stream);
 
+
+/*
+ * ts_lm_head_argmax — per-row argmax of the target LM head, computed in the epilogue of the
+ * LM-head GEMM so that the [M, N] logits are never written to HBM.
+ *
+ * Source: "jialefu.github.io — EAGLE-4 efficient LM head", section "A variant based on local
+ * Top-k" (selection fused with the vocabulary-tile matrix multiplication, scores kept on chip,
+ * the tiles' winners merged); for top-1 the merge is exact.  Consumed by the greedy check of
+ * "lesty.tech — EAGLE-2 vs. Medusa", section 4.
+ *
+ * logits[r][n] = sum_k hidden[r][k] * weight[n][k], bf16 inputs, fp32 accumulation (tensor
+ * cores; the summation order is the hardware's).  argmax[r] = the first n with the largest
+ * logit (ties -> lowest n); max_logit[r] (optional, NULL ok) = that logit.
+ * hidden  [M, K] bf16, device, 16-byte aligned.   weight [N, K] bf16 (one row per vocabulary
+ * entry, the usual LM-head layout), device, 16-byte aligned.   K % 8 == 0.
+ * argmax [M] int32, max_logit [M] fp32: device outputs.  workspace: caller-owned device
+ * memory of ts_lm_head_argmax_workspace(M, N, K) bytes.  Two launches on `stream`.
+ * Errors: TS_ERR_INVALID (sizes, alignment, null pointers), TS_ERR_WORKSPACE (too small)
+ * before any launch; TS_ERR_CUDA if a launch or the tensor-map encoding fails; a pipeline
+ * wait that times out sets *dev_status to TS_ERR_TIMEOUT.
+ */
+size_t ts_lm_head_argmax_workspace(int M, int N, int K);
+int ts_lm_head_argmax(const void* hidden, const void* weight, int M, int N, int K, int32_t* argmax,
+                      float* max_logit, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                      void* stream);
+
+/*
+ * ts_tree_accept_hidden — ts_tree_accept starting from the target's final hidden states
+ * instead of its logits: the per-node argmax comes from the fused LM-head GEMM above (no
+ * logits in HBM), then the same acceptance walk.  hidden [B, m, K] bf16, weight [V, K] bf16;
+ * other arguments and outputs as ts_tree_accept.  Workspace: ts_tree_accept_hidden_workspace.
+ */
+size_t ts_tree_accept_hidden_workspace(int B, int m, int V, int K);
+int ts_tree_accept_hidden(const void* hidden, const void* weight, const int32_t* tokens,
+                          const int32_t* parents, int B, int m, int V, int K, int32_t* argmax,
+                          int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
+                          size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /*
  * ts_kv_commit — after ts_tree_accept, keep the accepted path's K/V rows in the paged cache
  * and release the scratch pages that held only rejected tree nodes.

@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "TreeSpecError", "library", "library_path", "launch_count", "status_string",
-    "tree_build", "tree_attention", "tree_accept", "kv_commit", "new_status", "check_status",
+    "tree_build", "tree_attention", "tree_accept", "kv_commit", "lm_head_argmax", "tree_accept_hidden",
+    "new_status", "check_status",
     "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace", "tree_attention_plan",
 ]
 
@@ -69,6 +70,14 @@ def library():
         L.ts_tree_accept_workspace.argtypes = [I, I, I, I]
         L.ts_tree_accept.restype = I
         L.ts_tree_accept.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, S, P, P]
+        L.ts_lm_head_argmax_workspace.restype = S
+        L.ts_lm_head_argmax_workspace.argtypes = [I, I, I]
+        L.ts_lm_head_argmax.restype = I
+        L.ts_lm_head_argmax.argtypes = [P, P, I, I, I, P, P, P, S, P, P]
+        L.ts_tree_accept_hidden_workspace.restype = S
+        L.ts_tree_accept_hidden_workspace.argtypes = [I, I, I, I]
+        L.ts_tree_accept_hidden.restype = I
+        L.ts_tree_accept_hidden.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, S, P, P]
         L.ts_kv_commit.restype = I
         L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L
@@ -282,4 +291,55 @@ def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.T
     _check(L.ts_kv_commit(_p(k_cache), _p(v_cache), _dt(k_cache), nb, bs, hkv, d, _p(block_table), max_blocks,
                           _p(prefix_len), _p(accept_path), _p(accept_len), B, m, _p(out["freed_blocks"]),
                           _p(out["freed_count"]), _p(status), _stream()))
+    return out
+
+
+def lm_head_argmax(hidden: torch.Tensor, weight: torch.Tensor, *, out: Optional[Dict[str, torch.Tensor]] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """Per-row argmax (first index) and max of hidden [M,K] @ weight[N,K]^T (bf16), logits kept on chip."""
+    L = library()
+    _need_cuda("hidden", hidden, torch.bfloat16)
+    _need_cuda("weight", weight, torch.bfloat16)
+    M, K = hidden.shape
+    N, K2 = weight.shape
+    if K2 != K:
+        raise ValueError("hidden and weight disagree on K")
+    dev = hidden.device
+    if out is None:
+        out = dict(argmax=torch.empty(M, dtype=torch.int32, device=dev),
+                   max_logit=torch.empty(M, dtype=torch.float32, device=dev))
+    need = L.ts_lm_head_argmax_workspace(M, N, K)
+    if need == 0:
+        raise TreeSpecError("invalid lm_head_argmax sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_lm_head_argmax(_p(hidden), _p(weight), M, N, K, _p(out["argmax"]), _p(out.get("max_logit")), _p(ws),
+                               ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+def tree_accept_hidden(hidden: torch.Tensor, weight: torch.Tensor, tokens: torch.Tensor, parents: torch.Tensor, *,
+                       out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """tree_accept from the target's final hidden states [B,m,K] and its LM head [V,K] (bf16)."""
+    L = library()
+    _need_cuda("hidden", hidden, torch.bfloat16)
+    _need_cuda("weight", weight, torch.bfloat16)
+    _need_cuda("tokens", tokens, torch.int32)
+    _need_cuda("parents", parents, torch.int32)
+    B, m, K = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    if out is None:
+        out = dict(argmax=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   accept_path=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   bonus=torch.empty(B, dtype=torch.int32, device=dev))
+    need = L.ts_tree_accept_hidden_workspace(B, m, V, K)
+    if need == 0:
+        raise TreeSpecError("invalid tree_accept_hidden sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_tree_accept_hidden(_p(hidden), _p(weight), _p(tokens), _p(parents), B, m, V, K, _p(out["argmax"]),
+                                   _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws),
+                                   ws.numel() * ws.element_size(), _p(status), _stream()))
     return out

@@ -51,6 +51,8 @@ static int check_accept(ts_dtype dt, int B, int m, int V) {
 
 }  // namespace ts
 
+static bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 extern "C" {
 
 const char* ts_status_string(int status) {
@@ -167,6 +169,62 @@ int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
   return ts::tree_accept_launch(logits, dt, tokens, parents, B, m, V, argmax, accept_len,
                                 accept_path, bonus, workspace, dev_status,
                                 static_cast<cudaStream_t>(stream), sms);
+}
+
+static int check_lm_head(const void* hidden, const void* weight, long long M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0) return TS_ERR_INVALID;
+  if (!hidden || !weight || !aligned16_ptr(hidden) || !aligned16_ptr(weight)) return TS_ERR_INVALID;
+  if (M > (1LL << 24)) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+size_t ts_lm_head_argmax_workspace(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0) return 0;
+  return ts::lm_head_workspace_bytes(M, N, ts::device_sm_count());
+}
+
+int ts_lm_head_argmax(const void* hidden, const void* weight, int M, int N, int K, int32_t* argmax,
+                      float* max_logit, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                      void* stream) {
+  const int rc = check_lm_head(hidden, weight, M, N, K);
+  if (rc != TS_OK) return rc;
+  if (!argmax || !workspace) return TS_ERR_INVALID;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  if (ws_bytes < ts::lm_head_workspace_bytes(M, N, sms)) return TS_ERR_WORKSPACE;
+  return ts::lm_head_argmax_launch(hidden, weight, M, N, K, argmax, max_logit, workspace, dev_status,
+                                   static_cast<cudaStream_t>(stream), sms);
+}
+
+size_t ts_tree_accept_hidden_workspace(int B, int m, int V, int K) {
+  if (B <= 0 || m <= 0 || m > TS_MAX_NODES) return 0;
+  return ts_lm_head_argmax_workspace(B * m, V, K);
+}
+
+int ts_tree_accept_hidden(const void* hidden, const void* weight, const int32_t* tokens,
+                          const int32_t* parents, int B, int m, int V, int K, int32_t* argmax,
+                          int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
+                          size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (B <= 0 || m <= 0) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
+  const long long M = static_cast<long long>(B) * m;
+  const int rc = check_lm_head(hidden, weight, M, V, K);
+  if (rc != TS_OK) return rc;
+  if (!tokens || !parents || !argmax || !accept_len || !accept_path || !bonus || !workspace)
+    return TS_ERR_INVALID;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  const int Mi = static_cast<int>(M);
+  if (ws_bytes < ts::lm_head_workspace_bytes(Mi, V, sms)) return TS_ERR_WORKSPACE;
+  const int G = static_cast<int>(ts::lm_head_partials(Mi, V, sms));
+  float* part_v = static_cast<float*>(workspace);
+  int* part_i = reinterpret_cast<int*>(part_v + M * G);
+  int S = 0;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int r1 = ts::lm_head_partials_launch(hidden, weight, Mi, V, K, part_v, part_i, &S, dev_status, st, sms);
+  if (r1 != TS_OK) return r1;
+  return ts::accept_from_partials_launch(part_v, part_i, S, tokens, parents, B, m, argmax, accept_len,
+                                         accept_path, bonus, dev_status, st);
 }
 
 int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,

@@ -52,6 +52,20 @@ int attention_tc_launch(const AttnArgs& a, int num_sms);
 void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4);
 int attention_simt_launch(const AttnArgs& a);
 
+// accept_kernel on precomputed per-row partials (value, index) [B*m, S].
+int accept_from_partials_launch(const float* part_v, const int* part_i, int S, const int32_t* tokens,
+                                const int32_t* parents, int B, int m, int32_t* argmax, int32_t* accept_len,
+                                int32_t* accept_path, int32_t* bonus, int32_t* dev_status, cudaStream_t stream);
+
+// LM-head GEMM with the per-row argmax in its epilogue (lm_head.cu).
+size_t lm_head_partials(int M, int N, int num_sms);
+size_t lm_head_workspace_bytes(int M, int N, int num_sms);
+int lm_head_partials_launch(const void* hidden, const void* weight, int M, int N, int K, float* part_v,
+                            int* part_i, int* S_out, int32_t* dev_status, cudaStream_t stream, int num_sms);
+int lm_head_argmax_launch(const void* hidden, const void* weight, int M, int N, int K, int32_t* argmax,
+                          float* max_logit, void* workspace, int32_t* dev_status, cudaStream_t stream,
+                          int num_sms);
+
 int kv_commit_launch(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
                      int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
                      const int32_t* accept_path, const int32_t* accept_len, int B, int m,

@@ -1,0 +1,332 @@
+// ts_lm_head_argmax / ts_tree_accept_hidden: the target LM head's per-row argmax computed in
+// the epilogue of the LM-head GEMM, so the [rows, V] logits never reach HBM.
+//
+// Source: "jialefu.github.io — EAGLE-4 efficient LM head", section "A variant based on local
+// Top-k" (fuse the selection with the vocabulary-tile matrix multiplication and keep the
+// scores on chip; each tile keeps only its local winners and the tiles' winners are merged).
+// For top-1 the merge is exact: the row maximum is the maximum of the tiles' maxima, and the
+// lowest index among equal values survives when each tile reports its first maximum and the
+// merge breaks ties by index.  The greedy check that consumes it: "lesty.tech — EAGLE-2 vs.
+// Medusa", section 4.
+//
+// logits[r, n] = sum_k hidden[r, k] * weight[n, k] (bf16 inputs, fp32 accumulation on the
+// tensor cores).  CTA (mt, g) owns rows [128 mt, 128 mt + 128) and the vocabulary tiles
+// [g * tpg, (g + 1) * tpg) of 256 columns; it leaves one (max, first index) per row.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: per (tile, 64-wide K chunk) one 128x64 box of hidden and one
+//               256x64 box of weight (128-byte swizzle) into a 4-stage ring; rows past M or N
+//               and columns past K read zeros.
+//   warp 1      TMEM allocator + the MMA-issuing thread: tcgen05.mma kind::f16, M=128, N=256,
+//               four K=16 steps per chunk, into one of two 256-column accumulators, so the
+//               next tile's MMAs run while the previous tile's epilogue reads its accumulator.
+//   warps 2..5  epilogue, one thread per row (warp w reads TMEM lanes 32 (w % 4) ..): running
+//               maximum over the tile's columns in increasing order (strict > keeps the first
+//               index), columns past N skipped.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ts {
+namespace lm {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;      // two accumulators
+constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
+// full[ST] empty[ST] acc_full[2] acc_empty[2] drain
+constexpr int NBAR = 2 * STAGES + 5;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Wait bounded by time only (the abort path: let in-flight copies and MMAs land).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    lm_head_argmax_kernel(const __grid_constant__ CUtensorMap tma_h, const __grid_constant__ CUtensorMap tma_w,
+                          int M, int N, int K, int tpg, float* __restrict__ part_v, int* __restrict__ part_i,
+                          int S, int32_t* status) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* sptr = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, g = blockIdx.y;
+  const int NT = (N + BN - 1) / BN;
+  const int tile0 = g * tpg;
+  const int ntile = max(0, min(NT, tile0 + tpg) - tile0);
+  const int KC = (K + BK - 1) / BK;
+
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
+  auto full = [&](int s) { return bar(s); };
+  auto empty = [&](int s) { return bar(STAGES + s); };
+  auto acc_full = [&](int b) { return bar(2 * STAGES + b); };
+  auto acc_empty = [&](int b) { return bar(2 * STAGES + 2 + b); };
+  const uint32_t drain = bar(2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  pdl_wait();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int n0 = (tile0 + i) * BN;
+        for (int kc = 0; kc < KC; ++kc) {
+          const int it = i * KC + kc, s = it % STAGES;
+          if (it >= STAGES && !mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, status)) break;
+          mbar_expect_tx(full(s), STAGE_BYTES);
+          const uint32_t dst = sbase + s * STAGE_BYTES;
+          tma_load_2d(dst, &tma_h, full(s), kc * BK, mt * BM);
+          tma_load_2d(dst + A_BYTES, &tma_w, full(s), kc * BK, n0);
+          issued = it + 1;
+        }
+        if (*abort_flag) break;
+      }
+      if (*abort_flag) {
+        for (int it = max(0, issued - STAGES); it < issued; ++it) drain_wait(full(it % STAGES), (it / STAGES) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      bool ok = true;
+      for (int i = 0; i < ntile && ok; ++i) {
+        const int ab = i & 1;
+        if (i >= 2 && !mbar_wait(acc_empty(ab), ((i >> 1) - 1) & 1, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + ab * BN;
+        for (int kc = 0; kc < KC; ++kc) {
+          const int it = i * KC + kc, s = it % STAGES;
+          if (!mbar_wait(full(s), (it / STAGES) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_s = sbase + s * STAGE_BYTES, b_s = a_s + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_s + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_s + kk * 32, 16, 1024);
+            mma_ss(d, ad, bd, idesc, (kc | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty(s));
+        }
+        if (!ok) break;
+        tc_commit(acc_full(ab));
+      }
+      if (*abort_flag) {
+        // one more commit covers every MMA issued so far: TMEM is released only after them
+        tc_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;            // row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float best = -INFINITY;
+    int best_i = INT_MAX;
+    for (int i = 0; i < ntile; ++i) {
+      const int ab = i & 1;
+      if (!mbar_wait_warp(acc_full(ab), (i >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      const int n0 = (tile0 + i) * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + ab * BN + 32u * c, u);
+        const int nb = n0 + 32 * c;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float v = __uint_as_float(u[j]);
+          if (nb + j < N && v > best) {
+            best = v;
+            best_i = nb + j;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(ab));
+    }
+    const int row = mt * BM + r;
+    if (row < M && !*abort_flag) {
+      part_v[static_cast<long long>(row) * S + g] = best;
+      part_i[static_cast<long long>(row) * S + g] = best_i;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Merge the S partials of each row: first index among equal maxima.
+__global__ void __launch_bounds__(256) lm_head_merge_kernel(const float* __restrict__ part_v,
+                                                            const int* __restrict__ part_i, int S, int M,
+                                                            int32_t* __restrict__ argmax, float* __restrict__ max_logit) {
+  pdl_wait();
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  for (int s = 0; s < S; ++s) {
+    const float v = part_v[static_cast<long long>(row) * S + s];
+    const int i = part_i[static_cast<long long>(row) * S + s];
+    if (better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+  argmax[row] = bi;
+  if (max_logit != nullptr) max_logit[row] = bv;
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
+
+// [rows, K] bf16 row-major, boxes of box_rows x 64 with 128-byte swizzle.
+static bool encode_rows(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Vocabulary tiles per CTA: with MT row tiles, about one wave of CTAs (the MT CTAs of one
+// vocabulary range are adjacent in launch order, so they share the weight tiles in L2).
+static void plan(int M, int N, int num_sms, int* groups, int* tpg) {
+  const int MT = (M + BM - 1) / BM;
+  const int NT = (N + BN - 1) / BN;
+  int G = num_sms / MT;
+  if (G < 1) G = 1;
+  if (G > NT) G = NT;
+  const int t = (NT + G - 1) / G;
+  *tpg = t;
+  *groups = (NT + t - 1) / t;
+}
+
+}  // namespace lm
+
+size_t lm_head_partials(int M, int N, int num_sms) {
+  int G, t;
+  lm::plan(M, N, num_sms, &G, &t);
+  return static_cast<size_t>(G);
+}
+
+size_t lm_head_workspace_bytes(int M, int N, int num_sms) {
+  return static_cast<size_t>(M) * lm_head_partials(M, N, num_sms) * 8 + 256;
+}
+
+int lm_head_partials_launch(const void* hidden, const void* weight, int M, int N, int K, float* part_v,
+                            int* part_i, int* S_out, int32_t* dev_status, cudaStream_t stream, int num_sms) {
+  int G, tpg;
+  lm::plan(M, N, num_sms, &G, &tpg);
+  CUtensorMap mh, mw;
+  if (!lm::encode_rows(&mh, hidden, M, K, lm::BM) || !lm::encode_rows(&mw, weight, N, K, lm::BN))
+    return TS_ERR_CUDA;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(lm::lm_head_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    lm::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return TS_ERR_CUDA;
+  const int MT = (M + lm::BM - 1) / lm::BM;
+  if (launch_pdl(lm::lm_head_argmax_kernel, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, N, K,
+                 tpg, part_v, part_i, G, dev_status) != cudaSuccess)
+    return TS_ERR_CUDA;
+  count_launches(1);
+  *S_out = G;
+  return TS_OK;
+}
+
+int lm_head_argmax_launch(const void* hidden, const void* weight, int M, int N, int K, int32_t* argmax,
+                          float* max_logit, void* workspace, int32_t* dev_status, cudaStream_t stream,
+                          int num_sms) {
+  const int G = static_cast<int>(lm_head_partials(M, N, num_sms));
+  float* part_v = static_cast<float*>(workspace);
+  int* part_i = reinterpret_cast<int*>(part_v + static_cast<size_t>(M) * G);
+  int S = 0;
+  const int rc = lm_head_partials_launch(hidden, weight, M, N, K, part_v, part_i, &S, dev_status, stream, num_sms);
+  if (rc != TS_OK) return rc;
+  if (launch_pdl(lm::lm_head_merge_kernel, dim3((M + 255) / 256), dim3(256), 0, stream, part_v, part_i, S, M, argmax,
+                 max_logit) != cudaSuccess)
+    return TS_ERR_CUDA;
+  count_launches(1);
+  return TS_OK;
+}
+
+}  // namespace ts

@@ -247,6 +247,16 @@ static void accept_plan(ts_dtype dt, int B, int m, int V, int num_sms, int* S_ou
   *seg_out = seg;
 }
 
+int accept_from_partials_launch(const float* part_v, const int* part_i, int S, const int32_t* tokens,
+                                const int32_t* parents, int B, int m, int32_t* argmax, int32_t* accept_len,
+                                int32_t* accept_path, int32_t* bonus, int32_t* dev_status, cudaStream_t stream) {
+  if (launch_pdl(accept_kernel, dim3(B), dim3(kAcceptThreads), 0, stream, part_v, part_i, S, tokens, parents, m,
+                 argmax, accept_len, accept_path, bonus, dev_status) != cudaSuccess)
+    return TS_ERR_CUDA;
+  count_launches(1);
+  return TS_OK;
+}
+
 size_t tree_accept_workspace_bytes(ts_dtype dt, int B, int m, int V, int num_sms) {
   int S, seg;
   accept_plan(dt, B, m, V, num_sms, &S, &seg);
