@@ -13,6 +13,8 @@ Plain, slow, obviously-correct numpy restatements of what the pages define:
   scratch pages ("lesty.tech", section 8).
 * :mod:`oracle.lm_head`      — the target LM head's per-row argmax ("jialefu.github.io —
   EAGLE-4 efficient LM head", local Top-k section; "lesty.tech", section 4).
+* :mod:`oracle.efficient_head` — the draft's two-stage efficient LM head (low-rank scores,
+  local top-k per vocabulary tile, exact logits of the candidates; same page).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
@@ -27,3 +29,4 @@ from .tree_attention import tree_attention  # noqa: F401
 from .tree_accept import target_argmax, accept_longest_path  # noqa: F401
 from .kv_commit import kv_commit  # noqa: F401
 from .lm_head import lm_head_logits, lm_head_argmax, fp32_error_bound  # noqa: F401
+from .efficient_head import candidates, efficient_head  # noqa: F401
