@@ -345,7 +345,8 @@ def run_ours(args, rank, world, dev):
                      "frac": round(achieved_gbs / peak, 4), "traffic": traffic},
     }
     res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world),
-                        "lm_head_argmax": run_lm_head(w, args, flush, stream, dev)}
+                        "lm_head_argmax": run_lm_head(w, args, flush, stream, dev),
+                        "efficient_head": run_efficient_head(w, args, flush, stream, dev)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(step, w, ab, args, dev, world)
     return res, w, inp
@@ -400,6 +401,44 @@ def run_lm_head(w, args, flush, stream, dev):
     return {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": K}, "algorithmic_bytes": int(byts),
             "tb_s": round(tb_s, 4), "tflops": round(tflops, 2), "bound": bound, "frac_of_measured_peak": round(frac, 4),
             "logits_bytes_not_written": int(M * V * 4)}
+
+
+def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, k_tile=2):
+    """One draft step of the two-stage efficient head (the row after the hot path): the B*k
+    frontier rows of a drafter with a d_model-wide hidden state, seeded Gaussian bf16 factors;
+    rank, tile size and candidates per tile are a reading (the page states none)."""
+    import speculative_decoding_tree_eagle_gb300 as ts
+    d = D_MODEL.get(w.name.split("_prefix")[0], 4096)
+    M, V, k = w.B * w.k, w.V, w.k
+    g = torch.Generator(device=dev).manual_seed(20260 + 98)
+    h = torch.randn(M, d, generator=g, device=dev).to(torch.bfloat16)
+    B = (torch.randn(rank, d, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    A = (torch.randn(V, rank, generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    L = ts.library()
+    ws = torch.empty(max(256, L.ts_efficient_head_workspace(M, V, d, rank, tile_tokens, k_tile)), dtype=torch.uint8,
+                     device=dev)
+    status = ts.new_status(dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ts.efficient_head(h, B, A, W, tile_tokens=tile_tokens, k_tile=k_tile, k=k, workspace=ws, status=status)
+        b.record(stream)
+        if i >= args.warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    ts.check_status(status)
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    C = L.ts_efficient_head_candidates(V, tile_tokens, k_tile)
+    byts = (V * rank + rank * d + M * d) * 2 + M * C * d * 2 + M * k * 8
+    full_head = V * d * 2
+    del h, B, A, W
+    return {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": d, "rank": rank, "tile_tokens": tile_tokens,
+                                          "k_tile": k_tile, "candidates": C, "k": k},
+            "algorithmic_bytes": int(byts), "tb_s": round(byts / (ms * 1e-3) / 1e12, 4),
+            "full_head_bytes": int(full_head), "bound": "hbm (low-rank head + gathered candidate rows)"}
 
 
 def run_kv_commit(step, w, args, flush, stream, world):

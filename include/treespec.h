@@ -240,6 +240,49 @@ int ts_tree_accept_hidden(const void* hidden, const void* weight, const int32_t*
                           int32_t* accept_len, int32_t* accept_path, int32_t* bonus, void* workspace,
                           size_t ws_bytes, int32_t* dev_status, void* stream);
 
+
+/*
+ * ts_efficient_head — the draft model's two-stage efficient LM head.
+ *
+ * Source: "jialefu.github.io — EAGLE-4 efficient LM head", sections "EAGLE Efficient LM Head"
+ * (a low-rank head scores the whole vocabulary cheaply and candidates are chosen by top-k;
+ * the full LM-head rows of the candidates are gathered and their logits recomputed from the
+ * hidden states) and "A variant based on local Top-k" (the selection is fused into the
+ * vocabulary-tile matrix multiplication, each tile keeping its own k_tile best).
+ *
+ * Per row r of hidden [M, d]:  u = bf16(lr_b @ h)  (lr_b [rank, d]);  scores = lr_a @ u
+ * (lr_a [V, rank], fp32 accumulation, never written to HBM);  the vocabulary is cut into tiles
+ * of tile_tokens ids and each keeps its k_tile best (score descending, ties -> lower id) ->
+ * candidates [M, C], C = ts_efficient_head_candidates(V, tile_tokens, k_tile) (-1 in empty
+ * slots);  logits[c] = weight[c] @ h (weight [V, d], fp32);  top_tok [M, k] = the k best
+ * candidates (logit descending, ties -> lower id), top_logp [M, k] = logit - logsumexp over
+ * the candidates' logits.  Rows of top_tok / top_logp are what ts_tree_build_from_topk reads.
+ * All bf16 tensors row-major, device, 16-byte aligned; d % 8 == 0, rank % 8 == 0,
+ * tile_tokens % 256 == 0, 1 <= k_tile <= 8, 1 <= k <= min(16, C).  candidates may be NULL.
+ * Four launches on `stream`; workspace of ts_efficient_head_workspace(...) bytes.
+ * Errors: TS_ERR_INVALID / TS_ERR_UNSUPPORTED / TS_ERR_WORKSPACE before any launch;
+ * TS_ERR_CUDA on a launch or tensor-map failure; a timed-out pipeline wait sets *dev_status.
+ */
+int ts_efficient_head_candidates(int V, int tile_tokens, int k_tile);
+size_t ts_efficient_head_workspace(int M, int V, int d, int rank, int tile_tokens, int k_tile);
+int ts_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M,
+                      int V, int d, int rank, int tile_tokens, int k_tile, int k, int32_t* top_tok,
+                      float* top_logp, int32_t* candidates, void* workspace, size_t ws_bytes,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * ts_tree_build_from_topk — ts_tree_build starting from each draft row's top-k list instead of
+ * the full rows (for a drafter whose head already returns the top-k, such as
+ * ts_efficient_head): row_tok / row_logp [B, 1 + (depth-1) k, k], each row in order (value
+ * descending, ties -> lower token; a row out of order sets *dev_status to
+ * TS_ERR_DEVICE_CHECK and the sequence's outputs are not written).  Expansion, rerank,
+ * flatten and mask as ts_tree_build.  One launch; no workspace.
+ */
+int ts_tree_build_from_topk(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens,
+                            int B, int k, int depth, int m, int32_t* tokens, int32_t* parents,
+                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* dev_status,
+                            void* stream);
+
 /*
  * ts_kv_commit — after ts_tree_accept, keep the accepted path's K/V rows in the paged cache
  * and release the scratch pages that held only rejected tree nodes.

@@ -23,6 +23,7 @@ import torch
 __all__ = [
     "TreeSpecError", "library", "library_path", "launch_count", "status_string",
     "tree_build", "tree_attention", "tree_accept", "kv_commit", "lm_head_argmax", "tree_accept_hidden",
+    "efficient_head", "tree_build_from_topk",
     "new_status", "check_status",
     "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace", "tree_attention_plan",
 ]
@@ -78,6 +79,14 @@ def library():
         L.ts_tree_accept_hidden_workspace.argtypes = [I, I, I, I]
         L.ts_tree_accept_hidden.restype = I
         L.ts_tree_accept_hidden.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, S, P, P]
+        L.ts_efficient_head_candidates.restype = I
+        L.ts_efficient_head_candidates.argtypes = [I, I, I]
+        L.ts_efficient_head_workspace.restype = S
+        L.ts_efficient_head_workspace.argtypes = [I, I, I, I, I, I]
+        L.ts_efficient_head.restype = I
+        L.ts_efficient_head.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, S, P, P]
+        L.ts_tree_build_from_topk.restype = I
+        L.ts_tree_build_from_topk.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P]
         L.ts_kv_commit.restype = I
         L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L
@@ -342,4 +351,55 @@ def tree_accept_hidden(hidden: torch.Tensor, weight: torch.Tensor, tokens: torch
     _check(L.ts_tree_accept_hidden(_p(hidden), _p(weight), _p(tokens), _p(parents), B, m, V, K, _p(out["argmax"]),
                                    _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws),
                                    ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+def efficient_head(hidden: torch.Tensor, lr_b: torch.Tensor, lr_a: torch.Tensor, weight: torch.Tensor, *,
+                   tile_tokens: int, k_tile: int, k: int, with_candidates: bool = False,
+                   workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """Two-stage draft head: hidden [M,d], lr_b [rank,d], lr_a [V,rank], weight [V,d] (bf16) ->
+    top_tok [M,k], top_logp [M,k] (log-probs over the candidates), optionally candidates [M,C]."""
+    L = library()
+    for n, t in (("hidden", hidden), ("lr_b", lr_b), ("lr_a", lr_a), ("weight", weight)):
+        _need_cuda(n, t, torch.bfloat16)
+    M, d = hidden.shape
+    rank = lr_b.shape[0]
+    V = weight.shape[0]
+    dev = hidden.device
+    C = L.ts_efficient_head_candidates(V, tile_tokens, k_tile)
+    out = dict(top_tok=torch.empty(M, k, dtype=torch.int32, device=dev),
+               top_logp=torch.empty(M, k, dtype=torch.float32, device=dev))
+    if with_candidates:
+        out["candidates"] = torch.empty(M, max(C, 1), dtype=torch.int32, device=dev)
+    need = L.ts_efficient_head_workspace(M, V, d, rank, tile_tokens, k_tile)
+    if need == 0:
+        raise TreeSpecError("invalid efficient_head sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_efficient_head(_p(hidden), _p(lr_b), _p(lr_a), _p(weight), M, V, d, rank, tile_tokens, k_tile, k,
+                               _p(out["top_tok"]), _p(out["top_logp"]), _p(out.get("candidates")), _p(ws),
+                               ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+def tree_build_from_topk(row_tok: torch.Tensor, row_logp: torch.Tensor, root_tokens: torch.Tensor, k: int,
+                         depth: int, m: int, *, out: Optional[Dict[str, torch.Tensor]] = None,
+                         status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """tree_build from per-row top-k lists row_tok [B,R,k] int32 / row_logp [B,R,k] fp32."""
+    L = library()
+    _need_cuda("row_tok", row_tok, torch.int32)
+    _need_cuda("row_logp", row_logp, torch.float32)
+    _need_cuda("root_tokens", root_tokens, torch.int32)
+    B = row_tok.shape[0]
+    dev = row_tok.device
+    W = (m + 63) // 64
+    if out is None:
+        out = dict(tokens=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   parents=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   depth=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   mask=torch.empty(B, m, W, dtype=torch.int64, device=dev),
+                   values=torch.empty(B, m, dtype=torch.float64, device=dev))
+    _check(L.ts_tree_build_from_topk(_p(row_tok), _p(row_logp), _p(root_tokens), B, k, depth, m, _p(out["tokens"]),
+                                     _p(out["parents"]), _p(out["depth"]), _p(out["mask"]), _p(out.get("values")),
+                                     _p(status), _stream()))
     return out

@@ -227,6 +227,59 @@ int ts_tree_accept_hidden(const void* hidden, const void* weight, const int32_t*
                                          accept_path, bonus, dev_status, st);
 }
 
+int ts_efficient_head_candidates(int V, int tile_tokens, int k_tile) {
+  if (V <= 0 || tile_tokens <= 0 || tile_tokens % 256 != 0 || k_tile < 1 || k_tile > 8) return 0;
+  return ts::efficient_head_candidates(V, tile_tokens, k_tile);
+}
+
+static int check_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M,
+                                int V, int d, int rank, int tile_tokens, int k_tile, int k) {
+  if (M <= 0 || V <= 0 || d <= 0 || rank <= 0 || d % 8 != 0 || rank % 8 != 0) return TS_ERR_INVALID;
+  if (tile_tokens <= 0 || tile_tokens % 256 != 0 || k_tile < 1 || k_tile > tile_tokens) return TS_ERR_INVALID;
+  if (k_tile > 8 || k < 1 || k > TS_MAX_TOPK) return TS_ERR_UNSUPPORTED;
+  const long long C = static_cast<long long>((V + tile_tokens - 1) / tile_tokens) * k_tile;
+  if (k > C) return TS_ERR_INVALID;
+  if (C * 8 > 200 * 1024 || M > 65535) return TS_ERR_UNSUPPORTED;
+  if (!hidden || !lr_b || !lr_a || !weight) return TS_ERR_INVALID;
+  if (!aligned16_ptr(hidden) || !aligned16_ptr(lr_b) || !aligned16_ptr(lr_a) || !aligned16_ptr(weight))
+    return TS_ERR_INVALID;
+  return TS_OK;
+}
+
+size_t ts_efficient_head_workspace(int M, int V, int d, int rank, int tile_tokens, int k_tile) {
+  const void* p = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (check_efficient_head(p, p, p, p, M, V, d, rank, tile_tokens, k_tile, 1) != TS_OK) return 0;
+  return ts::efficient_head_workspace_bytes(M, V, rank, tile_tokens, k_tile);
+}
+
+int ts_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M,
+                      int V, int d, int rank, int tile_tokens, int k_tile, int k, int32_t* top_tok,
+                      float* top_logp, int32_t* candidates, void* workspace, size_t ws_bytes,
+                      int32_t* dev_status, void* stream) {
+  const int rc = check_efficient_head(hidden, lr_b, lr_a, weight, M, V, d, rank, tile_tokens, k_tile, k);
+  if (rc != TS_OK) return rc;
+  if (!top_tok || !top_logp || !workspace) return TS_ERR_INVALID;
+  if (ws_bytes < ts::efficient_head_workspace_bytes(M, V, rank, tile_tokens, k_tile)) return TS_ERR_WORKSPACE;
+  const int sms = ts::device_sm_count();
+  if (sms <= 0) return TS_ERR_CUDA;
+  return ts::efficient_head_launch(hidden, lr_b, lr_a, weight, M, V, d, rank, tile_tokens, k_tile, k, top_tok,
+                                   top_logp, candidates, workspace, dev_status, static_cast<cudaStream_t>(stream),
+                                   sms);
+}
+
+int ts_tree_build_from_topk(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens,
+                            int B, int k, int depth, int m, int32_t* tokens, int32_t* parents,
+                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* dev_status,
+                            void* stream) {
+  if (B <= 0 || k <= 0 || depth <= 0 || m <= 0) return TS_ERR_INVALID;
+  if (k > TS_MAX_TOPK || depth > TS_MAX_DEPTH || m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
+  const long long ncand = k + static_cast<long long>(depth - 1) * k * k;
+  if (m - 1 > ncand) return TS_ERR_INVALID;
+  if (!row_tok || !row_logp || !root_tokens || !tokens || !parents || !depth_out || !mask) return TS_ERR_INVALID;
+  return ts::tree_build_from_topk_launch(row_tok, row_logp, root_tokens, B, k, depth, m, tokens, parents, depth_out,
+                                         mask, values, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
                  int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
                  const int32_t* accept_path, const int32_t* accept_len, int B, int m,

@@ -66,6 +66,17 @@ int lm_head_argmax_launch(const void* hidden, const void* weight, int M, int N, 
                           float* max_logit, void* workspace, int32_t* dev_status, cudaStream_t stream,
                           int num_sms);
 
+int tree_build_from_topk_launch(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens, int B,
+                                int k, int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
+                                uint64_t* mask, double* values, int32_t* dev_status, cudaStream_t stream);
+
+int efficient_head_candidates(int V, int tile_tokens, int k_tile);
+size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile);
+int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M, int V,
+                          int d, int rank, int tile_tokens, int k_tile, int k, int32_t* top_tok, float* top_logp,
+                          int32_t* cand_out, void* workspace, int32_t* dev_status, cudaStream_t stream,
+                          int num_sms);
+
 int kv_commit_launch(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
                      int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
                      const int32_t* accept_path, const int32_t* accept_len, int B, int m,

@@ -65,10 +65,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// KT == 0: running (max, first index) over the CTA's columns -> part_v / part_i [M, S].
+// KT >= 1: the KT best columns (value descending, ties -> lower index) of every vocabulary tile
+// of vt consecutive 256-column tiles -> cand [M, C] at KT * (vocabulary tile) (-1 where a tile
+// has fewer columns); the CTA's tile range starts on a vocabulary-tile boundary.
+template <int KT>
 __global__ void __launch_bounds__(THREADS, 1)
-    lm_head_argmax_kernel(const __grid_constant__ CUtensorMap tma_h, const __grid_constant__ CUtensorMap tma_w,
-                          int M, int N, int K, int tpg, float* __restrict__ part_v, int* __restrict__ part_i,
-                          int S, int32_t* status) {
+    lm_head_kernel(const __grid_constant__ CUtensorMap tma_h, const __grid_constant__ CUtensorMap tma_w,
+                   int M, int N, int K, int tpg, float* __restrict__ part_v, int* __restrict__ part_i,
+                   int S, int vt, int32_t* __restrict__ cand, int C, int32_t* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -175,8 +180,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int r = q * 32 + lane;            // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    float best = -INFINITY;
-    int best_i = INT_MAX;
+    constexpr int KL = KT > 0 ? KT : 1;
+    float lv[KL];
+    int li[KL];
+#pragma unroll
+    for (int e = 0; e < KL; ++e) {
+      lv[e] = -INFINITY;
+      li[e] = INT_MAX;
+    }
+    const int row = mt * BM + r;
     for (int i = 0; i < ntile; ++i) {
       const int ab = i & 1;
       if (!mbar_wait_warp(acc_full(ab), (i >> 1) & 1, abort_flag, status)) break;
@@ -189,21 +201,49 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nb = n0 + 32 * c;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float v = __uint_as_float(u[j]);
-          if (nb + j < N && v > best) {
-            best = v;
-            best_i = nb + j;
+          float cv = __uint_as_float(u[j]);
+          if (nb + j < N && cv > lv[KL - 1]) {
+            // columns arrive in increasing order: a strict > keeps the earlier of equal values
+            // insert before the first smaller entry; everything after it shifts down by one
+            int ci = nb + j;
+            bool shift = false;
+#pragma unroll
+            for (int e = 0; e < KL; ++e) {
+              if (shift || cv > lv[e]) {
+                const float tv = lv[e];
+                const int ti = li[e];
+                lv[e] = cv;
+                li[e] = ci;
+                cv = tv;
+                ci = ti;
+                shift = true;
+              }
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(ab));
+      if (KT > 0) {
+        const int t = tile0 + i;
+        if ((t + 1) % vt == 0 || t == NT - 1) {  // a vocabulary tile ends here
+          if (row < M && !*abort_flag) {
+            const long long o = static_cast<long long>(row) * C + static_cast<long long>(t / vt) * KL;
+#pragma unroll
+            for (int e = 0; e < KL; ++e) cand[o + e] = li[e] == INT_MAX ? -1 : li[e];
+          }
+#pragma unroll
+          for (int e = 0; e < KL; ++e) {
+            lv[e] = -INFINITY;
+            li[e] = INT_MAX;
+          }
+        }
+      }
     }
-    const int row = mt * BM + r;
-    if (row < M && !*abort_flag) {
-      part_v[static_cast<long long>(row) * S + g] = best;
-      part_i[static_cast<long long>(row) * S + g] = best_i;
+    if (KT == 0 && row < M && !*abort_flag) {
+      part_v[static_cast<long long>(row) * S + g] = lv[0];
+      part_i[static_cast<long long>(row) * S + g] = li[0];
     }
   }
   tc_fence_before();
@@ -234,6 +274,156 @@ __global__ void __launch_bounds__(256) lm_head_merge_kernel(const float* __restr
   }
   argmax[row] = bi;
   if (max_logit != nullptr) max_logit[row] = bv;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The draft's two-stage efficient LM head ("jialefu.github.io — EAGLE-4 efficient LM head",
+// sections "EAGLE Efficient LM Head" and "A variant based on local Top-k"):
+//   u = bf16(B h) (lowrank_proj_kernel), scores = A u with the k_tile best ids of every
+//   vocabulary tile kept in the GEMM epilogue (lm_head_kernel<KT>), exact logits W[c] h of the
+//   candidates (gather_logits_kernel), and the k best candidates with log-probabilities over
+//   the candidate set (head_topk_kernel).
+// ---------------------------------------------------------------------------------------------
+
+// One warp per output u[row][j] = sum_k B[j][k] h[row][k] (fp32, lanes over 8-element chunks,
+// then a shuffle sum), rounded to bf16.  d % 8 == 0.
+__global__ void __launch_bounds__(256) lowrank_proj_kernel(const __nv_bfloat16* __restrict__ hidden,
+                                                          const __nv_bfloat16* __restrict__ lr_b, int d, int rank,
+                                                          __nv_bfloat16* __restrict__ u) {
+  pdl_wait();
+  const int row = blockIdx.x, j = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (j >= rank) return;
+  const uint4* h4 = reinterpret_cast<const uint4*>(hidden + static_cast<long long>(row) * d);
+  const uint4* b4 = reinterpret_cast<const uint4*>(lr_b + static_cast<long long>(j) * d);
+  float acc = 0.f;
+  for (int c = lane; c < d / 8; c += 32) {
+    const uint4 x = __ldg(h4 + c), y = __ldg(b4 + c);
+    acc = fmaf(bf16_lo(x.x), bf16_lo(y.x), acc);
+    acc = fmaf(bf16_hi(x.x), bf16_hi(y.x), acc);
+    acc = fmaf(bf16_lo(x.y), bf16_lo(y.y), acc);
+    acc = fmaf(bf16_hi(x.y), bf16_hi(y.y), acc);
+    acc = fmaf(bf16_lo(x.z), bf16_lo(y.z), acc);
+    acc = fmaf(bf16_hi(x.z), bf16_hi(y.z), acc);
+    acc = fmaf(bf16_lo(x.w), bf16_lo(y.w), acc);
+    acc = fmaf(bf16_hi(x.w), bf16_hi(y.w), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) u[static_cast<long long>(row) * rank + j] = __float2bfloat16_rn(acc);
+}
+
+// One warp per candidate: logits[row][c] = W[cand] . h[row] (fp32), -inf for an empty slot.
+__global__ void __launch_bounds__(256) gather_logits_kernel(const __nv_bfloat16* __restrict__ hidden,
+                                                           const __nv_bfloat16* __restrict__ weight, int V, int d,
+                                                           const int32_t* __restrict__ cand, int C,
+                                                           float* __restrict__ logits, int32_t* status) {
+  pdl_wait();
+  const int row = blockIdx.x, c = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const int id = cand[static_cast<long long>(row) * C + c];
+  float acc = -INFINITY;
+  if (id >= 0 && id < V) {
+    const uint4* h4 = reinterpret_cast<const uint4*>(hidden + static_cast<long long>(row) * d);
+    const uint4* w4 = reinterpret_cast<const uint4*>(weight + static_cast<long long>(id) * d);
+    acc = 0.f;
+    for (int k = lane; k < d / 8; k += 32) {
+      const uint4 x = __ldg(h4 + k), y = __ldg(w4 + k);
+      acc = fmaf(bf16_lo(x.x), bf16_lo(y.x), acc);
+      acc = fmaf(bf16_hi(x.x), bf16_hi(y.x), acc);
+      acc = fmaf(bf16_lo(x.y), bf16_lo(y.y), acc);
+      acc = fmaf(bf16_hi(x.y), bf16_hi(y.y), acc);
+      acc = fmaf(bf16_lo(x.z), bf16_lo(y.z), acc);
+      acc = fmaf(bf16_hi(x.z), bf16_hi(y.z), acc);
+      acc = fmaf(bf16_lo(x.w), bf16_lo(y.w), acc);
+      acc = fmaf(bf16_hi(x.w), bf16_hi(y.w), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  } else if (id >= V && lane == 0) {
+    report(status, TS_ERR_DEVICE_CHECK);
+  }
+  if (lane == 0) logits[static_cast<long long>(row) * C + c] = acc;
+}
+
+// One CTA per row: the k best candidates (logit descending, ties -> lower id) and their
+// log-probabilities over the candidate set (logit - logsumexp of the candidates' logits).
+constexpr int kHeadThreads = 256;
+__device__ __forceinline__ void block_best_pair(float& v, int& i, float* s_v, int* s_i) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    s_v[warp] = v;
+    s_i[warp] = i;
+  }
+  __syncthreads();
+  v = s_v[0];
+  i = s_i[0];
+  for (int w = 1; w < kHeadThreads / 32; ++w)
+    if (better(s_v[w], s_i[w], v, i)) {
+      v = s_v[w];
+      i = s_i[w];
+    }
+}
+
+__global__ void __launch_bounds__(kHeadThreads) head_topk_kernel(const float* __restrict__ logits,
+                                                                const int32_t* __restrict__ cand, int C, int k,
+                                                                int32_t* __restrict__ top_tok,
+                                                                float* __restrict__ top_logp) {
+  extern __shared__ unsigned char smem_raw[];
+  float* sl = reinterpret_cast<float*>(smem_raw);
+  int* si = reinterpret_cast<int*>(sl + C);
+  __shared__ float s_v[kHeadThreads / 32];
+  __shared__ int s_i[kHeadThreads / 32];
+  pdl_wait();
+  const int row = blockIdx.x;
+  float mx = -INFINITY;
+  for (int c = threadIdx.x; c < C; c += kHeadThreads) {
+    const int id = cand[static_cast<long long>(row) * C + c];
+    const float l = logits[static_cast<long long>(row) * C + c];
+    sl[c] = id >= 0 ? l : -INFINITY;
+    si[c] = id >= 0 ? id : INT_MAX;
+    mx = fmaxf(mx, sl[c]);
+  }
+  int dummy = 0;
+  block_best_pair(mx, dummy, s_v, s_i);
+  float sum = 0.f;
+  for (int c = threadIdx.x; c < C; c += kHeadThreads)
+    if (sl[c] != -INFINITY) sum += expf(sl[c] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_v[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < kHeadThreads / 32; ++w) tot += s_v[w];
+  const float lse = mx + logf(tot);
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX, bc = -1;
+    for (int c = threadIdx.x; c < C; c += kHeadThreads)
+      if (better(sl[c], si[c], bv, bi)) {
+        bv = sl[c];
+        bi = si[c];
+        bc = c;
+      }
+    int who = bi;
+    block_best_pair(bv, who, s_v, s_i);
+    if (bi == who && bc >= 0 && who != INT_MAX) sl[bc] = -INFINITY, si[bc] = INT_MAX;  // take it out
+    if (threadIdx.x == 0) {
+      top_tok[static_cast<long long>(row) * k + j] = who == INT_MAX ? -1 : who;
+      top_logp[static_cast<long long>(row) * k + j] = who == INT_MAX ? -INFINITY : bv - lse;
+    }
+    __syncthreads();
+  }
 }
 
 using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -267,13 +457,14 @@ static bool encode_rows(CUtensorMap* map, const void* base, int rows, int K, int
 
 // Vocabulary tiles per CTA: with MT row tiles, about one wave of CTAs (the MT CTAs of one
 // vocabulary range are adjacent in launch order, so they share the weight tiles in L2).
-static void plan(int M, int N, int num_sms, int* groups, int* tpg) {
+static void plan(int M, int N, int num_sms, int* groups, int* tpg, int vt = 1) {
   const int MT = (M + BM - 1) / BM;
   const int NT = (N + BN - 1) / BN;
+  const int NV = (NT + vt - 1) / vt;  // vocabulary tiles; a CTA takes whole ones
   int G = num_sms / MT;
   if (G < 1) G = 1;
-  if (G > NT) G = NT;
-  const int t = (NT + G - 1) / G;
+  if (G > NV) G = NV;
+  const int t = (NV + G - 1) / G * vt;
   *tpg = t;
   *groups = (NT + t - 1) / t;
 }
@@ -300,13 +491,13 @@ int lm_head_partials_launch(const void* hidden, const void* weight, int M, int N
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(lm::lm_head_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(lm::lm_head_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     lm::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return TS_ERR_CUDA;
   const int MT = (M + lm::BM - 1) / lm::BM;
-  if (launch_pdl(lm::lm_head_argmax_kernel, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, N, K,
-                 tpg, part_v, part_i, G, dev_status) != cudaSuccess)
+  if (launch_pdl(lm::lm_head_kernel<0>, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, N, K,
+                 tpg, part_v, part_i, G, 1, static_cast<int32_t*>(nullptr), 0, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   count_launches(1);
   *S_out = G;
@@ -326,6 +517,83 @@ int lm_head_argmax_launch(const void* hidden, const void* weight, int M, int N, 
                  max_logit) != cudaSuccess)
     return TS_ERR_CUDA;
   count_launches(1);
+  return TS_OK;
+}
+
+
+int efficient_head_candidates(int V, int tile_tokens, int k_tile) {
+  return (V + tile_tokens - 1) / tile_tokens * k_tile;
+}
+
+size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile) {
+  const size_t C = static_cast<size_t>(efficient_head_candidates(V, tile_tokens, k_tile));
+  const size_t u = (static_cast<size_t>(M) * rank * 2 + 255) / 256 * 256;
+  return u + static_cast<size_t>(M) * C * 8 + 256;
+}
+
+template <int KT>
+static cudaError_t launch_scores(const CUtensorMap& mh, const CUtensorMap& mw, int M, int V, int rank, int tpg,
+                                 int G, int vt, int32_t* cand, int C, int32_t* status, cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(lm::lm_head_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    lm::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int MT = (M + lm::BM - 1) / lm::BM;
+  return launch_pdl(lm::lm_head_kernel<KT>, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, V,
+                    rank, tpg, static_cast<float*>(nullptr), static_cast<int*>(nullptr), 0, vt, cand, C, status);
+}
+
+int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M, int V,
+                          int d, int rank, int tile_tokens, int k_tile, int k, int32_t* top_tok, float* top_logp,
+                          int32_t* cand_out, void* workspace, int32_t* dev_status, cudaStream_t stream,
+                          int num_sms) {
+  const int C = efficient_head_candidates(V, tile_tokens, k_tile);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(ws);
+  const size_t u_bytes = (static_cast<size_t>(M) * rank * 2 + 255) / 256 * 256;
+  int32_t* cand = cand_out != nullptr ? cand_out : reinterpret_cast<int32_t*>(ws + u_bytes);
+  float* logits = reinterpret_cast<float*>(ws + u_bytes + static_cast<size_t>(M) * C * 4);
+  // 1. u = bf16(B h)
+  if (launch_pdl(lm::lowrank_proj_kernel, dim3(M, (rank + 7) / 8), dim3(256), 0, stream,
+                 static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(lr_b), d, rank, u) !=
+      cudaSuccess)
+    return TS_ERR_CUDA;
+  // 2. scores = A u with the local top-k_tile of every vocabulary tile
+  const int vt = tile_tokens / lm::BN;
+  int G, tpg;
+  lm::plan(M, V, num_sms, &G, &tpg, vt);
+  CUtensorMap mu, ma;
+  if (!lm::encode_rows(&mu, u, M, rank, lm::BM) || !lm::encode_rows(&ma, lr_a, V, rank, lm::BN)) return TS_ERR_CUDA;
+  cudaError_t e;
+  switch (k_tile) {
+    case 1: e = launch_scores<1>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 2: e = launch_scores<2>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 3: e = launch_scores<3>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 4: e = launch_scores<4>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 5: e = launch_scores<5>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 6: e = launch_scores<6>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 7: e = launch_scores<7>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    default: e = launch_scores<8>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+  }
+  if (e != cudaSuccess) return TS_ERR_CUDA;
+  // 3. exact logits of the candidates
+  if (launch_pdl(lm::gather_logits_kernel, dim3(M, (C + 7) / 8), dim3(256), 0, stream,
+                 static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(weight), V, d, cand, C,
+                 logits, dev_status) != cudaSuccess)
+    return TS_ERR_CUDA;
+  // 4. the k best candidates and their log-probabilities over the candidate set
+  const size_t smem = static_cast<size_t>(C) * 8;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(lm::head_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+    return TS_ERR_CUDA;
+  if (launch_pdl(lm::head_topk_kernel, dim3(M), dim3(lm::kHeadThreads), smem, stream, logits, cand, C, k, top_tok,
+                 top_logp) != cudaSuccess)
+    return TS_ERR_CUDA;
+  count_launches(4);
   return TS_OK;
 }
 

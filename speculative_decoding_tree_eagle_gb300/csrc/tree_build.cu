@@ -362,6 +362,17 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     }
     for (int x = tid; x < depth + 2; x += kTreeThreads) cnt[x] = 0;
     __syncthreads();
+    // every row list must be in order (value descending, ties -> lower token), as the row
+    // streams and the efficient head emit them
+    for (int e = tid; e < R * k; e += kTreeThreads) {
+      if (e % k == 0) continue;
+      if (rlp[e - 1] < rlp[e] || (rlp[e - 1] == rlp[e] && rtok[e - 1] > rtok[e])) *err = 1;
+    }
+    __syncthreads();
+    if (*err) {
+      if (tid == 0) report(status, TS_ERR_DEVICE_CHECK);
+      return;
+    }
 
     // 2. Expansion, layer by layer: value = parent value + log-prob (fp64, root -> leaf);
     //    frontier slot j of layer l-1 is the candidate of rank j in that layer.  A candidate's
@@ -607,4 +618,20 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
+
+int tree_build_from_topk_launch(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens, int B,
+                                int k, int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
+                                uint64_t* mask, double* values, int32_t* dev_status, cudaStream_t stream) {
+  const int R = 1 + (depth - 1) * k;
+  const int W = (m + 63) / 64;
+  const TreeSmem L = tree_smem_layout(k, depth, R, m);
+  if (L.total > 48 * 1024 &&
+      cudaFuncSetAttribute(tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
+    return TS_ERR_CUDA;
+  if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), L.total, stream, row_logp, row_tok, root_tokens, R, k,
+                 depth, m, W, tokens, parents, depth_out, mask, values, dev_status) != cudaSuccess)
+    return TS_ERR_CUDA;
+  count_launches(1);
+  return TS_OK;
+}
 }  // namespace ts
