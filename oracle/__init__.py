@@ -30,3 +30,4 @@ from .tree_accept import target_argmax, accept_longest_path  # noqa: F401
 from .kv_commit import kv_commit  # noqa: F401
 from .lm_head import lm_head_logits, lm_head_argmax, fp32_error_bound  # noqa: F401
 from .efficient_head import candidates, efficient_head  # noqa: F401
+from .accept_sample import accept_sample, softmax_t  # noqa: F401

@@ -28,6 +28,10 @@ Readings where the pages are silent (each listed in the design notes):
 * flatten order: root first, then by (depth, parent's flat index, child rank), which
   reproduces the page's worked sequence;
 * the root is node 0 with value 0 and is always kept; ``m`` counts the root.
+* ``node_row`` names, per flattened node, the draft row its children were drawn from
+  (root: row 0; an expanded frontier node of layer l in slot j: ``1 + (l-1)*k + j``; -1
+  for a node that was never expanded).  Stochastic verification needs it: the draft
+  distribution q at a node is that row.
 
 Pins (tests/test_oracle_tree_build.py, tests/test_oracle_mask.py): the page's worked
 mask row, a hand-built case that must reproduce the page's tree and order, the product
@@ -59,6 +63,7 @@ class _Cand:
     parent: int    # candidate id of the parent, -1 for the root
     rank: int      # rank among the parent's k children
     value: float   # V = V(parent) + log p, fp64, accumulated root -> leaf
+    slot: int = -1  # position in its layer's frontier (expanded), -1 if never expanded
 
 
 def _expand(logp: np.ndarray, k: int, depth: int) -> List[_Cand]:
@@ -72,6 +77,8 @@ def _expand(logp: np.ndarray, k: int, depth: int) -> List[_Cand]:
         layer.append(len(cands) - 1)
     frontier = sorted(layer, key=lambda x: (-cands[x].value, cands[x].idx))[:k]
     for l in range(2, depth + 1):
+        for j, par in enumerate(frontier):
+            cands[par].slot = j
         layer = []
         for j, par in enumerate(frontier):
             ids, lps = topk[1 + (l - 2) * k + j]
@@ -149,26 +156,31 @@ def tree_build_one(logp: np.ndarray, root_token: int, k: int, depth: int, m: int
     parents = np.zeros(m, dtype=np.int64)
     depth_out = np.zeros(m, dtype=np.int64)
     values = np.zeros(m, dtype=np.float64)
+    node_row = np.full(m, -1, dtype=np.int64)
     tokens[0], parents[0], depth_out[0], values[0] = root_token, -1, 0, 0.0
+    if m > 1:
+        node_row[0] = 0
     for pos, x in enumerate(seq, start=1):
         c = cands[x]
         tokens[pos] = c.token
         parents[pos] = 0 if c.parent == -1 else flat[c.parent]
         depth_out[pos] = c.layer
         values[pos] = c.value
+        if c.slot >= 0:
+            node_row[pos] = 1 + (c.layer - 1) * k + c.slot
     mask = ancestor_mask(parents)
-    return dict(tokens=tokens, parents=parents, depth=depth_out, values=values,
+    return dict(tokens=tokens, parents=parents, depth=depth_out, values=values, node_row=node_row,
                 mask=mask, mask_words=mask_to_words(mask), n_candidates=len(cands))
 
 
 def tree_build(draft_logp, root_tokens, k: int, depth: int, m: int) -> dict:
     """Batched tree construction.  ``draft_logp``: [B, 1+(depth-1)k, V] fp32 log-probs.
 
-    Returns int64 ``tokens``, ``parents``, ``depth`` [B, m], fp64 ``values`` [B, m],
+    Returns int64 ``tokens``, ``parents``, ``depth``, ``node_row`` [B, m], fp64 ``values`` [B, m],
     bool ``mask`` [B, m, m] and uint64 ``mask_words`` [B, m, ceil(m/64)].
     """
     logp = np.asarray(draft_logp, dtype=np.float32)
     roots = np.asarray(root_tokens).astype(np.int64)
     per = [tree_build_one(logp[b], int(roots[b]), k, depth, m) for b in range(logp.shape[0])]
     return {key: np.stack([p[key] for p in per]) for key in
-            ("tokens", "parents", "depth", "values", "mask", "mask_words")}
+            ("tokens", "parents", "depth", "values", "node_row", "mask", "mask_words")}

@@ -164,3 +164,36 @@ def test_workload_batch_shapes():
     out = tree_build(inp["draft_logp"].numpy(), inp["root_tokens"].numpy(), w.k, w.depth, w.m)
     assert out["tokens"].shape == (w.B, w.m) and out["mask_words"].shape == (w.B, w.m, 1)
     assert out["tokens"][0, 0] == int(inp["root_tokens"][0])
+
+
+@pytest.mark.parametrize("k,depth,m", [(2, 3, 8), (3, 4, 20), (4, 5, 40), (1, 6, 7), (5, 3, 31)])
+def test_node_row_names_the_row_that_drew_the_children(k, depth, m):
+    """Each row's top-k lives in its own block of token ids (row r owns ids r*k .. r*k+k-1), so
+    the row a node's children came from can be read off the children's tokens, with no
+    frontier bookkeeping.  A node that was expanded carries that row; every other node -1."""
+    R = 1 + (depth - 1) * k
+    V = R * k + 16
+    rng = np.random.default_rng(k * 100 + depth * 10 + m)
+    logp = np.full((R, V), -30.0)
+    for r in range(R):
+        logp[r, r * k:(r + 1) * k] = np.log(rng.dirichlet(np.ones(k)) * 0.9)
+    logp = logp.astype(np.float32)
+    out = tree_build_one(logp, V - 1, k, depth, m)
+    rows_seen = {}
+    for i in range(1, m):
+        rows_seen.setdefault(int(out["parents"][i]), set()).add(int(out["tokens"][i]) // k)
+    expanded = 0
+    for p in range(m):
+        if p in rows_seen:
+            assert rows_seen[p] == {int(out["node_row"][p])}
+        if out["node_row"][p] >= 0:
+            expanded += 1
+            assert out["depth"][p] < depth
+    # rows are distinct, the root uses row 0, and no more rows than were drawn
+    rows = [int(r) for r in out["node_row"] if r >= 0]
+    assert len(rows) == len(set(rows)) and out["node_row"][0] == 0 and expanded <= R
+
+
+def test_node_row_root_only():
+    out = tree_build_one(np.zeros((1, 4), np.float32), 3, 2, 1, 1)
+    assert out["node_row"].tolist() == [-1]
