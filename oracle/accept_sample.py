@@ -39,11 +39,11 @@ Readings (the page prints no tree form; each is listed in the design notes):
   A proposal whose remaining mass is zero stays zero, so the next test reads 0 < p(x).
 
 Outputs per sequence: accept_len (nodes on the kept path, root included), accept_path
-(flat indices, then -1) and bonus (the drawn token).  ``margin`` is the distance of every
-decision taken from its threshold (|r - p(x)/q(x)| for trials, the distance of the
-inverse-CDF target to the drawn token's cumulative bounds for the bonus), the minimum over
-the step: a GPU path computing p in fp32 may take a different branch only where it is
-small.
+(flat indices, then -1) and bonus (the drawn token).  Two margins say how close the step came
+to another outcome: ``margin`` = min over the trials taken of |r - p(x)/q(x)| (inf without
+trials) and ``bonus_margin`` = the distance of the inverse-CDF target r * total to the drawn
+token's cumulative bounds, over the total.  A GPU path computing p in fp32 may take another
+branch only where one of them is small.
 
 Pins (tests/test_oracle_accept_sample.py): the first emitted token is distributed as p
 (exact enumeration over uniforms on a grid for a small chain, a chi-square test on trees in
@@ -91,7 +91,8 @@ def _draw(p: np.ndarray, r: float):
 def accept_sample_one(logits, tokens, parents, uniforms, temperature: float, q_mode: str = "point",
                       draft_rows=None, node_row=None):
     """One sequence.  ``logits`` [m, V]; ``draft_rows`` [R, V] fp32 log-probs and ``node_row``
-    [m] are needed for q_mode "draft".  Returns (accept_len, path list, bonus, margin)."""
+    [m] are needed for q_mode "draft".  Returns (accept_len, path list, bonus, margin,
+    bonus_margin)."""
     if q_mode not in ("point", "draft"):
         raise ValueError("q_mode is 'point' or 'draft'")
     L = _f64(logits)
@@ -134,7 +135,7 @@ def accept_sample_one(logits, tokens, parents, uniforms, temperature: float, q_m
                     q = q / q.sum()
         if kept is None:
             bonus, mb = _draw(p, r[0])
-            return len(path), path, bonus, min(margin, mb)
+            return len(path), path, bonus, margin, mb
         path.append(kept)
         u = kept
 
@@ -145,18 +146,19 @@ def accept_sample(logits, tokens, parents, uniforms, temperature: float, q_mode:
     ``draft_logp`` [B, R, V] and ``node_row`` [B, m] for q_mode "draft".
 
     Returns int64 accept_len [B], accept_path [B, m] (-1 padded), bonus [B] and fp64
-    margin [B]."""
+    margin [B] and bonus_margin [B]."""
     L = _f64(logits)
     B, m = L.shape[0], L.shape[1]
     alen = np.zeros(B, dtype=np.int64)
     apath = np.full((B, m), -1, dtype=np.int64)
     bonus = np.zeros(B, dtype=np.int64)
     margin = np.zeros(B)
+    bmargin = np.zeros(B)
     for b in range(B):
-        a, path, y, mg = accept_sample_one(
+        a, path, y, mg, mb = accept_sample_one(
             L[b], np.asarray(tokens)[b], np.asarray(parents)[b], np.asarray(uniforms)[b], temperature, q_mode,
             None if draft_logp is None else np.asarray(draft_logp)[b],
             None if node_row is None else np.asarray(node_row)[b])
-        alen[b], bonus[b], margin[b] = a, y, mg
+        alen[b], bonus[b], margin[b], bmargin[b] = a, y, mg, mb
         apath[b, :a] = path
-    return alen, apath, bonus, margin
+    return alen, apath, bonus, margin, bmargin

@@ -74,7 +74,7 @@ def test_first_and_second_tokens_follow_the_target(q_mode, T):
     for _ in range(N):
         tok = _sample_tokens(rng, q_mode, draft)
         u = rng.random(len(PARENTS))
-        a, path, y, _ = accept_sample_one(logits, tok, PARENTS, u, T, q_mode, draft, NODE_ROW)
+        a, path, y, _, _ = accept_sample_one(logits, tok, PARENTS, u, T, q_mode, draft, NODE_ROW)
         first[_emitted(a, path, y, tok, 1)] += 1
         if a >= 2 and path[1] == 1:
             second[_emitted(a, path, y, tok, 2)] += 1
@@ -94,7 +94,7 @@ def test_draft_proposals_with_fixed_children_are_not_lossless():
     N = 12000
     first = np.zeros(V)
     for _ in range(N):
-        a, path, y, _ = accept_sample_one(logits, tok, PARENTS, rng.random(len(PARENTS)), 1.0, "draft", draft,
+        a, path, y, _, _ = accept_sample_one(logits, tok, PARENTS, rng.random(len(PARENTS)), 1.0, "draft", draft,
                                           NODE_ROW)
         first[_emitted(a, path, y, tok, 1)] += 1
     assert chisquare(first, softmax_t(logits[0], 1.0) * N).pvalue < 1e-6
@@ -124,13 +124,13 @@ def test_one_candidate_chain_reproduces_the_page_formulas(q_mode):
     qx = q if q_mode == "draft" else qq
     kept = 0
     for r in _grid(G):
-        a, _, _, _ = accept_sample_one(lg, tok, par, np.array([0.5, r]), 1.0, q_mode, d, nr)
+        a, _, _, _, _ = accept_sample_one(lg, tok, par, np.array([0.5, r]), 1.0, q_mode, d, nr)
         kept += a == 2
     assert abs(kept / G - min(1.0, p[x] / qx[x])) <= 1.0 / G
     # residual: the child is rejected for r = 0.999999; sweep the bonus uniform
     hist = np.zeros(V)
     for r0 in _grid(G):
-        a, _, y, _ = accept_sample_one(lg, tok, par, np.array([r0, 0.999999]), 1.0, q_mode, d, nr)
+        a, _, y, _, _ = accept_sample_one(lg, tok, par, np.array([r0, 0.999999]), 1.0, q_mode, d, nr)
         assert a == 1
         hist[y] += 1
     expect = np.maximum(0.0, p - qx) / (1.0 - np.minimum(p, qx).sum())
@@ -144,7 +144,7 @@ def test_kept_child_takes_the_walk_down():
     par = np.array([-1, 0, 1, 1])
     tok = np.array([0, 2, 1, 3])
     nr = np.array([0, 1, -1, -1])
-    a, path, y, _ = accept_sample_one(lg, tok, par, np.array([0.3, 0.99, 0.99, 0.5]), 1.0, "draft", d, nr)
+    a, path, y, _, _ = accept_sample_one(lg, tok, par, np.array([0.3, 0.99, 0.99, 0.5]), 1.0, "draft", d, nr)
     assert a == 3 and path == [0, 1, 2]
 
 
@@ -154,7 +154,7 @@ def test_zero_target_mass_rejects_every_candidate():
     tok = np.array([0, 2, 3])
     for mode in ("point", "draft"):
         d = np.log(np.array([[0.1, 0.1, 0.4, 0.4]]))
-        a, path, y, _ = accept_sample_one(lg, tok, par, np.array([0.75, 0.0, 0.0]), 1.0, mode, d,
+        a, path, y, _, _ = accept_sample_one(lg, tok, par, np.array([0.75, 0.0, 0.0]), 1.0, mode, d,
                                           np.array([0, -1, -1]))
         assert a == 1 and y == 1                     # residual is p itself here: [0.5, 0.5, 0, 0]
 
@@ -179,7 +179,7 @@ def test_low_temperature_is_greedy():
                 want = (want + 1) % Vv
             used[p].add(want)
             tokens[b, i] = want
-    alen, apath, bonus, _ = accept_sample(logits, tokens, parents, rng.random((B, m)), 1e-6, "point")
+    alen, apath, bonus, _, _ = accept_sample(logits, tokens, parents, rng.random((B, m)), 1e-6, "point")
     ref = accept_longest_path(tokens, parents, amax)
     np.testing.assert_array_equal(alen, ref[0])
     np.testing.assert_array_equal(apath, ref[1])
@@ -191,10 +191,14 @@ def test_margin_is_the_distance_to_the_nearest_threshold():
     lg = np.log(np.array([[0.25, 0.25, 0.5], [1 / 3, 1 / 3, 1 / 3]]))
     par = np.array([-1, 0])
     tok = np.array([0, 2])
-    a, _, _, mg = accept_sample_one(lg, tok, par, np.array([0.1, 0.45]), 1.0, "point")
-    assert a == 2 and abs(mg - 0.05) < 1e-12   # trial: |0.45 - 0.5|; bonus at node 1: 0.1 in [0, 1/3)
-    a, _, y, mg = accept_sample_one(lg, tok, par, np.array([0.3, 0.6]), 1.0, "point")
-    assert a == 1 and y == 0 and abs(mg - 0.1) < 1e-12      # residual [.5, .5, 0]: 0.3 vs boundary 0.5
+    a, _, _, mg, mb = accept_sample_one(lg, tok, par, np.array([0.1, 0.45]), 1.0, "point")
+    assert a == 2 and abs(mg - 0.05) < 1e-12   # trial: |0.45 - 0.5|
+    assert abs(mb - 0.1) < 1e-12               # bonus at node 1: 0.1 in [0, 1/3)
+    a, _, y, mg, mb = accept_sample_one(lg, tok, par, np.array([0.3, 0.6]), 1.0, "point")
+    assert a == 1 and y == 0 and abs(mg - 0.1) < 1e-12      # trial: |0.6 - 0.5|
+    assert abs(mb - 0.2) < 1e-12                            # residual [.5, .5, 0]: 0.3 in [0, 0.5)
+    _, _, _, mg, _ = accept_sample_one(lg[:1], tok[:1], par[:1], np.array([0.3]), 1.0, "point")
+    assert mg == np.inf
 
 
 def test_bad_parents_raise():
