@@ -6,6 +6,7 @@
  *   ts_tree_build      dynamic draft-tree construction (expand, rerank, flatten, mask)
  *   ts_tree_attention  every tree node attends to the paged KV prefix + its own ancestors
  *   ts_tree_accept     per-node argmax of the target logits + longest matching root path
+ *   ts_tree_accept_sample  the same verification at temperature T > 0 (rejection sampling)
  *
  * Conventions shared by every entry point
  *   - Every tensor argument is a DEVICE pointer owned by the caller.  The library never
@@ -56,6 +57,11 @@ typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
 #define TS_MAX_NODES 256
 #define TS_MAX_TOPK 16
 #define TS_MAX_DEPTH 16
+/* ts_tree_accept_sample: V <= TS_SAMPLE_MAX_VOCAB. */
+#define TS_SAMPLE_MAX_VOCAB (1 << 20)
+
+/* Proposal q of ts_tree_accept_sample (see there). */
+typedef enum { TS_Q_POINT = 0, TS_Q_DRAFT = 1 } ts_q_mode;
 
 /* Human-readable name of a ts_status value (static string, never NULL). */
 const char* ts_status_string(int status);
@@ -89,6 +95,9 @@ uint64_t ts_launch_count(void);
  *   mask      uint64 [B, m, W]: bit (j % 64) of word j / 64 of row i is set iff node j is
  *             node i or one of its ancestors.
  *   values    fp64 (optional, NULL to skip): global value = summed log-probs, root 0.
+ *   node_row  int32 [B, m] (optional, NULL to skip): the draft row each node was expanded with
+ *             (0 for the root, 1 + (l-1)k + slot for frontier slot `slot` of layer l), -1 for
+ *             a node that was not expanded (it has no children).
  * Order of the flattened nodes: root, then by (depth, parent's flat index, rank of the
  * child within its parent's top-k).  Top-k ties -> lower token id; frontier ties -> lower
  * layer-local index; rerank ties -> shallower, then lower layer-local index.
@@ -99,7 +108,7 @@ size_t ts_tree_build_workspace(int B, int V, int k, int depth, int m);
 int ts_tree_build(const float* draft_logp, const int32_t* root_tokens,
                   int B, int V, int k, int depth, int m,
                   int32_t* tokens, int32_t* parents, int32_t* depth_out, uint64_t* mask,
-                  double* values,
+                  double* values, int32_t* node_row,
                   void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------------------
@@ -280,8 +289,8 @@ int ts_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, co
  */
 int ts_tree_build_from_topk(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens,
                             int B, int k, int depth, int m, int32_t* tokens, int32_t* parents,
-                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* dev_status,
-                            void* stream);
+                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* node_row,
+                            int32_t* dev_status, void* stream);
 
 /*
  * ts_kv_commit — after ts_tree_accept, keep the accepted path's K/V rows in the paged cache
@@ -319,6 +328,49 @@ int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int 
                  int Hkv, int d, int32_t* block_table, int max_blocks, int32_t* prefix_len,
                  const int32_t* accept_path, const int32_t* accept_len, int B, int m,
                  int32_t* freed_blocks, int32_t* freed_count, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * ts_tree_accept_sample — verification of the tree when the target samples at temperature
+ * T > 0: multi-round rejection sampling.
+ * Source: "lesty.tech — EAGLE-2 vs. Medusa", section 4 (Mathematical Verification: Lossless
+ * Rejection Sampling): a candidate x proposed by q is kept with probability min(1, p(x)/q(x));
+ * after a rejection one token is drawn from max(0, p - q) / (1 - sum min(p, q)).
+ *
+ * Per sequence, starting at the root: p = softmax(logits[node] / T).  The node's children
+ * are tried in increasing flat index; child c with token x is kept iff
+ * uniforms[b][c] * q(x) < p(x).  The first kept child becomes the current node.  After a
+ * rejection p becomes max(0, p - q) renormalised (unchanged if that has zero mass) and x
+ * leaves q (q(x) = 0, q renormalised).  When no child is kept (or there are none), one token
+ * is drawn from the current p by inverse CDF over increasing token ids with
+ * uniforms[b][0]: the smallest y whose cumulative mass exceeds uniforms[b][0] * total.
+ *   q_mode TS_Q_POINT: q is a unit mass on each candidate (the trial reads r < p(x), a
+ *     rejection removes x's mass from p).  Lossless for children chosen deterministically,
+ *     such as the draft's top-k of ts_tree_build.
+ *   q_mode TS_Q_DRAFT: q = exp(draft_logp[b][node_row[b][node]]) renormalised (the draft
+ *     row that proposed the node's children, as ts_tree_build's node_row output names it).
+ *     Lossless for children drawn from q without replacement.
+ *
+ * logits      [B, m, V] (dt), row (b, i) = target logits after node i's root path.
+ * tokens, parents [B, m] int32 (parents[0] == -1, parents[i] in [0, i); tokens in [0, V)).
+ * uniforms    [B, m] float, each in [0, 1): entry c decides the trial of child c (a node is
+ *             tried at most once), entry 0 draws the final token.
+ * draft_logp  [B, R, V] float log-probabilities, node_row [B, m] int32 — TS_Q_DRAFT only
+ *             (may be NULL for TS_Q_POINT); a node with children needs node_row in [0, R).
+ * temperature finite, > 0.
+ * Outputs: accept_len [B] (kept nodes, root included), accept_path [B, m] (flat indices from
+ * the root, then -1), bonus [B] (the drawn token).
+ * Workspace: ts_tree_accept_sample_workspace(B, V, q_mode) bytes (0 for TS_Q_POINT; the
+ * pointer may then be NULL).  Limits: m <= TS_MAX_NODES, V <= TS_SAMPLE_MAX_VOCAB.
+ * Device errors: a bad parent, token or node_row, or a target row without mass (every logit
+ * -inf or NaN) -> TS_ERR_DEVICE_CHECK; for a bad tree that sequence's outputs are
+ * accept_len 0, path all -1, bonus -1.  One launch, one CTA per sequence.
+ * --------------------------------------------------------------------------------- */
+size_t ts_tree_accept_sample_workspace(int B, int V, int q_mode);
+int ts_tree_accept_sample(const void* logits, ts_dtype dt, const int32_t* tokens, const int32_t* parents,
+                          const float* uniforms, const float* draft_logp, const int32_t* node_row, int R,
+                          int B, int m, int V, float temperature, int q_mode, int32_t* accept_len,
+                          int32_t* accept_path, int32_t* bonus, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

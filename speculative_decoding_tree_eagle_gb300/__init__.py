@@ -60,7 +60,7 @@ def library():
         L.ts_tree_build_workspace.restype = S
         L.ts_tree_build_workspace.argtypes = [I, I, I, I, I]
         L.ts_tree_build.restype = I
-        L.ts_tree_build.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P, S, P, P]
+        L.ts_tree_build.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P, P, S, P, P]
         L.ts_tree_attention_workspace.restype = S
         L.ts_tree_attention_workspace.argtypes = [I, I, I, I, I, I, I]
         L.ts_tree_attention.restype = I
@@ -86,7 +86,11 @@ def library():
         L.ts_efficient_head.restype = I
         L.ts_efficient_head.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, S, P, P]
         L.ts_tree_build_from_topk.restype = I
-        L.ts_tree_build_from_topk.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P]
+        L.ts_tree_build_from_topk.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
+        L.ts_tree_accept_sample_workspace.restype = S
+        L.ts_tree_accept_sample_workspace.argtypes = [I, I, I]
+        L.ts_tree_accept_sample.restype = I
+        L.ts_tree_accept_sample.argtypes = [P, I, P, P, P, P, P, I, I, I, I, F, I, P, P, P, P, S, P, P]
         L.ts_kv_commit.restype = I
         L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L
@@ -205,13 +209,14 @@ def tree_build(draft_logp: torch.Tensor, root_tokens: torch.Tensor, k: int, dept
                    mask=torch.empty(B, m, W, dtype=torch.int64, device=dev))
         if with_values:
             out["values"] = torch.empty(B, m, dtype=torch.float64, device=dev)
+        out["node_row"] = torch.empty(B, m, dtype=torch.int32, device=dev)
     need = L.ts_tree_build_workspace(B, V, k, depth, m)
     if need == 0:
         raise TreeSpecError("invalid tree_build sizes")
     ws = _workspace(need, dev, workspace)
     _check(L.ts_tree_build(_p(draft_logp), _p(root_tokens), B, V, k, depth, m, _p(out["tokens"]),
                            _p(out["parents"]), _p(out["depth"]), _p(out["mask"]), _p(out.get("values")),
-                           _p(ws), ws.numel() * ws.element_size(), _p(status), _stream()))
+                           _p(out.get("node_row")), _p(ws), ws.numel() * ws.element_size(), _p(status), _stream()))
     return out
 
 
@@ -273,6 +278,48 @@ def tree_accept(logits: torch.Tensor, tokens: torch.Tensor, parents: torch.Tenso
     _check(L.ts_tree_accept(_p(logits), dt, _p(tokens), _p(parents), B, m, V, _p(out["argmax"]),
                             _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws),
                             ws.numel() * ws.element_size(), _p(status), _stream()))
+    return out
+
+
+Q_MODES = {"point": 0, "draft": 1}
+
+
+def tree_accept_sample(logits: torch.Tensor, tokens: torch.Tensor, parents: torch.Tensor, uniforms: torch.Tensor,
+                       temperature: float, *, q_mode: str = "point", draft_logp: Optional[torch.Tensor] = None,
+                       node_row: Optional[torch.Tensor] = None, out: Optional[Dict[str, torch.Tensor]] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """Verification at temperature T > 0 by multi-round rejection sampling: logits [B,m,V],
+    tokens/parents [B,m] int32, uniforms [B,m] float32 in [0, 1).  q_mode "point" (a unit mass
+    per candidate) or "draft" (the draft rows draft_logp [B,R,V] named by node_row [B,m]).
+    Returns accept_len [B], accept_path [B,m] and bonus [B] (the drawn token)."""
+    L = library()
+    _need_cuda("logits", logits)
+    _need_cuda("tokens", tokens, torch.int32)
+    _need_cuda("parents", parents, torch.int32)
+    _need_cuda("uniforms", uniforms, torch.float32)
+    if q_mode not in Q_MODES:
+        raise TreeSpecError("q_mode is 'point' or 'draft'")
+    B, m, V = logits.shape
+    R = 0
+    if q_mode == "draft":
+        if draft_logp is None or node_row is None:
+            raise TreeSpecError("q_mode 'draft' needs draft_logp and node_row")
+        _need_cuda("draft_logp", draft_logp, torch.float32)
+        _need_cuda("node_row", node_row, torch.int32)
+        R = draft_logp.shape[1]
+    dev = logits.device
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   accept_path=torch.empty(B, m, dtype=torch.int32, device=dev),
+                   bonus=torch.empty(B, dtype=torch.int32, device=dev))
+    need = L.ts_tree_accept_sample_workspace(B, V, Q_MODES[q_mode])
+    ws = _workspace(need, dev, workspace) if need > 0 else None
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(L.ts_tree_accept_sample(_p(logits), _dt(logits), _p(tokens), _p(parents), _p(uniforms), _p(draft_logp),
+                                   _p(node_row), R, B, m, V, float(temperature), Q_MODES[q_mode],
+                                   _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws), nbytes,
+                                   _p(status), _stream()))
     return out
 
 
@@ -398,8 +445,9 @@ def tree_build_from_topk(row_tok: torch.Tensor, row_logp: torch.Tensor, root_tok
                    parents=torch.empty(B, m, dtype=torch.int32, device=dev),
                    depth=torch.empty(B, m, dtype=torch.int32, device=dev),
                    mask=torch.empty(B, m, W, dtype=torch.int64, device=dev),
-                   values=torch.empty(B, m, dtype=torch.float64, device=dev))
+                   values=torch.empty(B, m, dtype=torch.float64, device=dev),
+                   node_row=torch.empty(B, m, dtype=torch.int32, device=dev))
     _check(L.ts_tree_build_from_topk(_p(row_tok), _p(row_logp), _p(root_tokens), B, k, depth, m, _p(out["tokens"]),
                                      _p(out["parents"]), _p(out["depth"]), _p(out["mask"]), _p(out.get("values")),
-                                     _p(status), _stream()))
+                                     _p(out.get("node_row")), _p(status), _stream()))
     return out

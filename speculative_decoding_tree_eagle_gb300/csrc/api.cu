@@ -79,7 +79,7 @@ size_t ts_tree_build_workspace(int B, int V, int k, int depth, int m) {
 
 int ts_tree_build(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
                   int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
-                  uint64_t* mask, double* values, void* workspace, size_t ws_bytes,
+                  uint64_t* mask, double* values, int32_t* node_row, void* workspace, size_t ws_bytes,
                   int32_t* dev_status, void* stream) {
   const int rc = ts::check_build(B, V, k, depth, m);
   if (rc != TS_OK) return rc;
@@ -89,7 +89,7 @@ int ts_tree_build(const float* draft_logp, const int32_t* root_tokens, int B, in
   if (sms <= 0) return TS_ERR_CUDA;
   if (ws_bytes < ts::tree_build_workspace_bytes(B, V, k, depth, sms)) return TS_ERR_WORKSPACE;
   return ts::tree_build_launch(draft_logp, root_tokens, B, V, k, depth, m, tokens, parents,
-                               depth_out, mask, values, workspace, dev_status,
+                               depth_out, mask, values, node_row, workspace, dev_status,
                                static_cast<cudaStream_t>(stream), sms);
 }
 
@@ -269,15 +269,15 @@ int ts_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, co
 
 int ts_tree_build_from_topk(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens,
                             int B, int k, int depth, int m, int32_t* tokens, int32_t* parents,
-                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* dev_status,
-                            void* stream) {
+                            int32_t* depth_out, uint64_t* mask, double* values, int32_t* node_row,
+                            int32_t* dev_status, void* stream) {
   if (B <= 0 || k <= 0 || depth <= 0 || m <= 0) return TS_ERR_INVALID;
   if (k > TS_MAX_TOPK || depth > TS_MAX_DEPTH || m > TS_MAX_NODES) return TS_ERR_UNSUPPORTED;
   const long long ncand = k + static_cast<long long>(depth - 1) * k * k;
   if (m - 1 > ncand) return TS_ERR_INVALID;
   if (!row_tok || !row_logp || !root_tokens || !tokens || !parents || !depth_out || !mask) return TS_ERR_INVALID;
   return ts::tree_build_from_topk_launch(row_tok, row_logp, root_tokens, B, k, depth, m, tokens, parents, depth_out,
-                                         mask, values, dev_status, static_cast<cudaStream_t>(stream));
+                                         mask, values, node_row, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int block_size,
@@ -295,6 +295,30 @@ int ts_kv_commit(void* k_cache, void* v_cache, ts_dtype dt, int num_blocks, int 
   return ts::kv_commit_launch(k_cache, v_cache, dt, num_blocks, block_size, Hkv, d, block_table,
                               max_blocks, prefix_len, accept_path, accept_len, B, m, freed_blocks,
                               freed_count, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t ts_tree_accept_sample_workspace(int B, int V, int q_mode) {
+  if (B <= 0 || V <= 0 || (q_mode != TS_Q_POINT && q_mode != TS_Q_DRAFT)) return 0;
+  return ts::tree_accept_sample_workspace_bytes(B, V, q_mode);
+}
+
+int ts_tree_accept_sample(const void* logits, ts_dtype dt, const int32_t* tokens, const int32_t* parents,
+                          const float* uniforms, const float* draft_logp, const int32_t* node_row, int R,
+                          int B, int m, int V, float temperature, int q_mode, int32_t* accept_len,
+                          int32_t* accept_path, int32_t* bonus, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream) {
+  if (B <= 0 || m <= 0 || V <= 0) return TS_ERR_INVALID;
+  if (dt != TS_F32 && dt != TS_BF16) return TS_ERR_INVALID;
+  if (q_mode != TS_Q_POINT && q_mode != TS_Q_DRAFT) return TS_ERR_INVALID;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES || V > TS_SAMPLE_MAX_VOCAB || B > 65535) return TS_ERR_UNSUPPORTED;
+  if (!logits || !tokens || !parents || !uniforms || !accept_len || !accept_path || !bonus) return TS_ERR_INVALID;
+  if (q_mode == TS_Q_DRAFT && (!draft_logp || !node_row || R <= 0)) return TS_ERR_INVALID;
+  const size_t need = ts::tree_accept_sample_workspace_bytes(B, V, q_mode);
+  if (need > 0 && (!workspace || ws_bytes < need)) return workspace ? TS_ERR_WORKSPACE : TS_ERR_INVALID;
+  return ts::tree_accept_sample_launch(logits, dt, tokens, parents, uniforms, draft_logp, node_row, R, B, m, V,
+                                       temperature, q_mode, accept_len, accept_path, bonus, workspace, dev_status,
+                                       static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

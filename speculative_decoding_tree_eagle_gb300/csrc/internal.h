@@ -15,7 +15,7 @@ int device_sm_count();
 size_t tree_build_workspace_bytes(int B, int V, int k, int depth, int num_sms);
 int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
                       int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
-                      uint64_t* mask, double* values, void* workspace, int32_t* dev_status,
+                      uint64_t* mask, double* values, int32_t* node_row, void* workspace, int32_t* dev_status,
                       cudaStream_t stream, int num_sms);
 
 size_t tree_accept_workspace_bytes(ts_dtype dt, int B, int m, int V, int num_sms);
@@ -68,7 +68,16 @@ int lm_head_argmax_launch(const void* hidden, const void* weight, int M, int N, 
 
 int tree_build_from_topk_launch(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens, int B,
                                 int k, int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
-                                uint64_t* mask, double* values, int32_t* dev_status, cudaStream_t stream);
+                                uint64_t* mask, double* values, int32_t* node_row, int32_t* dev_status,
+                                cudaStream_t stream);
+
+// Stochastic verification by multi-round rejection sampling (tree_sample.cu).
+size_t tree_accept_sample_workspace_bytes(int B, int V, int q_mode);
+int tree_accept_sample_launch(const void* logits, ts_dtype dt, const int32_t* tokens, const int32_t* parents,
+                              const float* uniforms, const float* draft_logp, const int32_t* node_row, int R,
+                              int B, int m, int V, float temperature, int q_mode, int32_t* accept_len,
+                              int32_t* accept_path, int32_t* bonus, void* workspace, int32_t* dev_status,
+                              cudaStream_t stream);
 
 int efficient_head_candidates(int V, int tile_tokens, int k_tile);
 size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile);

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     const float* __restrict__ part_v, const int* __restrict__ part_i,
     const int32_t* __restrict__ root_tokens, int R, int k, int depth, int m, int W,
     int32_t* __restrict__ tokens, int32_t* __restrict__ parents, int32_t* __restrict__ depth_out,
-    uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* status) {
+    uint64_t* __restrict__ mask, double* __restrict__ values, int32_t* __restrict__ node_row, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_wait();
   const TreeSmem L = tree_smem_layout(k, depth, R, m);
@@ -517,8 +517,11 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
       fpar[f] = pf;
       tokens[out0 + f] = ctok[x];
       parents[out0 + f] = pf;
-      depth_out[out0 + f] = layer_of(x, k, depth);
+      const int lx = layer_of(x, k, depth);
+      depth_out[out0 + f] = lx;
       if (values) values[out0 + f] = cV[x];
+      // the draft row a node was expanded with: frontier slot lrank of layer lx (< depth)
+      if (node_row) node_row[out0 + f] = (lx < depth && lrank[x] < k) ? 1 + (lx - 1) * k + lrank[x] : -1;
     }
   }
   if (tid == 0) {
@@ -527,6 +530,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(
     parents[out0] = -1;
     depth_out[out0] = 0;
     if (values) values[out0] = 0.0;
+    if (node_row) node_row[out0] = m > 1 ? 0 : -1;
   }
   __syncthreads();
   // the next kernel's CTAs may be placed now: only the short mask pass is left
@@ -582,7 +586,7 @@ size_t tree_build_workspace_bytes(int B, int V, int k, int depth, int num_sms) {
 
 int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B, int V, int k,
                       int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
-                      uint64_t* mask, double* values, void* workspace, int32_t* dev_status,
+                      uint64_t* mask, double* values, int32_t* node_row, void* workspace, int32_t* dev_status,
                       cudaStream_t stream, int num_sms) {
   const int R = 1 + (depth - 1) * k;
   int S, seg;
@@ -611,7 +615,7 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
       return TS_ERR_CUDA;
   }
   if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), smem, stream, part_v, part_i, root_tokens, R, k,
-                 depth, m, W, tokens, parents, depth_out, mask, values, dev_status) != cudaSuccess)
+                 depth, m, W, tokens, parents, depth_out, mask, values, node_row, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   ++launches;
   count_launches(launches);
@@ -621,7 +625,8 @@ int tree_build_launch(const float* draft_logp, const int32_t* root_tokens, int B
 
 int tree_build_from_topk_launch(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens, int B,
                                 int k, int depth, int m, int32_t* tokens, int32_t* parents, int32_t* depth_out,
-                                uint64_t* mask, double* values, int32_t* dev_status, cudaStream_t stream) {
+                                uint64_t* mask, double* values, int32_t* node_row, int32_t* dev_status,
+                                cudaStream_t stream) {
   const int R = 1 + (depth - 1) * k;
   const int W = (m + 63) / 64;
   const TreeSmem L = tree_smem_layout(k, depth, R, m);
@@ -629,7 +634,7 @@ int tree_build_from_topk_launch(const int32_t* row_tok, const float* row_logp, c
       cudaFuncSetAttribute(tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
     return TS_ERR_CUDA;
   if (launch_pdl(tree_kernel, dim3(B), dim3(kTreeThreads), L.total, stream, row_logp, row_tok, root_tokens, R, k,
-                 depth, m, W, tokens, parents, depth_out, mask, values, dev_status) != cudaSuccess)
+                 depth, m, W, tokens, parents, depth_out, mask, values, node_row, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   count_launches(1);
   return TS_OK;

@@ -47,7 +47,7 @@ def test_status_strings(lib):
 
 def _build(lib, B=1, V=100, k=2, depth=3, m=8, ptr=1):
     P = ptr
-    return lib.ts_tree_build(P, P, B, V, k, depth, m, P, P, P, P, None, P, 1 << 20, None, None)
+    return lib.ts_tree_build(P, P, B, V, k, depth, m, P, P, P, P, None, None, P, 1 << 20, None, None)
 
 
 def test_tree_build_validation(lib):
@@ -107,6 +107,30 @@ def test_kv_commit_validation(lib):
     assert _commit(lib, d=3) == TS_ERR_INVALID          # bf16 rows of 6 bytes
     assert _commit(lib, m=257) == TS_ERR_UNSUPPORTED
     assert _commit(lib, ptr=None) == TS_ERR_INVALID
+
+
+def _sample(lib, dt=1, B=1, m=8, V=100, T=1.0, mode=0, R=3, ptr=1, draft=1, ws=None, wsb=0):
+    P = ptr
+    return lib.ts_tree_accept_sample(P, dt, P, P, P, draft, draft, R, B, m, V, T, mode, P, P, P, ws, wsb, None, None)
+
+
+def test_tree_accept_sample_validation(lib):
+    assert _sample(lib, B=0) == TS_ERR_INVALID
+    assert _sample(lib, V=0) == TS_ERR_INVALID
+    assert _sample(lib, dt=3) == TS_ERR_INVALID
+    assert _sample(lib, mode=2) == TS_ERR_INVALID
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert _sample(lib, T=T) == TS_ERR_INVALID
+    assert _sample(lib, m=257) == TS_ERR_UNSUPPORTED
+    assert _sample(lib, V=(1 << 20) + 1) == TS_ERR_UNSUPPORTED
+    assert _sample(lib, ptr=None) == TS_ERR_INVALID
+    assert _sample(lib, mode=1, draft=None) == TS_ERR_INVALID       # draft mode needs the rows
+    assert _sample(lib, mode=1, R=0) == TS_ERR_INVALID
+    assert _sample(lib, mode=1) == TS_ERR_INVALID                    # and a workspace
+    assert _sample(lib, mode=1, ws=1, wsb=16) == -3                  # too small
+    assert lib.ts_tree_accept_sample_workspace(1, 100, 0) == 0
+    assert lib.ts_tree_accept_sample_workspace(2, 100, 1) >= 2 * 2 * 104 * 4
+    assert lib.ts_tree_accept_sample_workspace(2, 100, 7) == 0
 
 
 def test_workspace_queries_are_positive_for_valid_sizes(lib):

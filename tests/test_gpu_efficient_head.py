@@ -81,7 +81,7 @@ def test_tree_from_topk_equals_tree_from_rows():
                                 roots.to(dev()), k, depth, m, status=status)
     bt = ts.tree_build(logp.to(dev()), roots.to(dev()), k, depth, m, status=status)
     ts.check_status(status)
-    for key in ("tokens", "parents", "depth", "mask", "values"):
+    for key in ("tokens", "parents", "depth", "mask", "values", "node_row"):
         assert torch.equal(a[key], bt[key]), key
 
 
@@ -115,7 +115,7 @@ def test_efficient_head_feeds_the_tree():
     tok = out["top_tok"].view(Bs, R, k).cpu().numpy()
     lp = out["top_logp"].view(Bs, R, k).cpu().numpy()
     ref = oracle.tree_build(_rows_from_lists(tok, lp, V), roots.numpy(), k, depth, m)
-    for key in ("tokens", "parents", "depth"):
+    for key in ("tokens", "parents", "depth", "node_row"):
         np.testing.assert_array_equal(tree[key].cpu().numpy(), ref[key])
     np.testing.assert_array_equal(tree["mask"].cpu().numpy().view(np.uint64), ref["mask_words"])
     np.testing.assert_array_equal(tree["values"].cpu().numpy(), ref["values"])

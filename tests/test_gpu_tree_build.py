@@ -22,7 +22,7 @@ def _run_and_compare(draft_logp: torch.Tensor, roots: torch.Tensor, k, depth, m,
     got = ts.tree_build(x, roots.to(dev()), k, depth, m, status=status)
     ts.check_status(status)
     ref = oracle.tree_build(draft_logp.numpy(), roots.numpy(), k, depth, m)
-    for key in ("tokens", "parents", "depth"):
+    for key in ("tokens", "parents", "depth", "node_row"):
         np.testing.assert_array_equal(got[key].cpu().numpy(), ref[key], err_msg=key)
     np.testing.assert_array_equal(got["mask"].cpu().numpy().view(np.uint64), ref["mask_words"])
     np.testing.assert_array_equal(got["values"].cpu().numpy(), ref["values"])
