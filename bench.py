@@ -175,7 +175,8 @@ class Step:
                          parents=torch.empty(B, m, dtype=torch.int32, device=dev),
                          depth=torch.empty(B, m, dtype=torch.int32, device=dev),
                          mask=torch.empty(B, m, W, dtype=torch.int64, device=dev),
-                         values=torch.empty(B, m, dtype=torch.float64, device=dev))
+                         values=torch.empty(B, m, dtype=torch.float64, device=dev),
+                         node_row=torch.empty(B, m, dtype=torch.int32, device=dev))
         self.out = torch.empty_like(self.d["q"])
         self.lse = torch.empty(B, m, w.Hq, dtype=torch.float32, device=dev)
         self.acc = dict(argmax=torch.empty(B, m, dtype=torch.int32, device=dev),
@@ -346,7 +347,8 @@ def run_ours(args, rank, world, dev):
     }
     res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world),
                         "lm_head_argmax": run_lm_head(w, args, flush, stream, dev),
-                        "efficient_head": run_efficient_head(w, args, flush, stream, dev)}
+                        "efficient_head": run_efficient_head(w, args, flush, stream, dev),
+                        "accept_sample": run_accept_sample(step, w, args, flush, stream, world)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(step, w, ab, args, dev, world)
     return res, w, inp
@@ -439,6 +441,77 @@ def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, 
                                           "k_tile": k_tile, "candidates": C, "k": k},
             "algorithmic_bytes": int(byts), "tb_s": round(byts / (ms * 1e-3) / 1e12, 4),
             "full_head_bytes": int(full_head), "bound": "hbm (low-rank head + gathered candidate rows)"}
+
+
+def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
+    """Verification at T > 0 by multi-round rejection sampling (the row after greedy
+    acceptance), both proposal modes, on the step's own tree.  Target logits: the step's
+    N(0,1) logits with one child of every expanded node raised to ln(V) + U(0, 4) (kept with
+    probability ~0.4..1 per level), so that walks go several levels deep as in the pages'
+    reported acceptance lengths; seeded uniforms.  L2 flushed before each call."""
+    ts = step.ts
+    d = step.d
+    B, m, V = w.B, w.m, w.V
+    tok, par, nrow = step.tree["tokens"], step.tree["parents"], step.tree["node_row"]
+    par_h, tok_h = par.cpu().numpy(), tok.cpu().numpy()
+    rng = np.random.default_rng(w.seed + 11)
+    bi, ui, ti, vals = [], [], [], []
+    for b in range(B):
+        for u in range(m):
+            kids = np.nonzero(par_h[b] == u)[0]
+            if len(kids):
+                bi.append(b), ui.append(u), ti.append(int(tok_h[b, kids[rng.integers(len(kids))]]))
+                vals.append(math.log(V) + rng.uniform(0.0, 4.0))
+    logits = d["logits"].clone()
+    dev = logits.device
+    idx = tuple(torch.tensor(x, dtype=torch.long, device=dev) for x in (bi, ui, ti))
+    logits.index_put_(idx, torch.tensor(vals, dtype=torch.float32, device=dev).to(logits.dtype))
+    g = torch.Generator(device=dev).manual_seed(w.seed + 12)
+    uniforms = torch.rand(B, m, generator=g, device=dev)
+    out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+               accept_path=torch.empty(B, m, dtype=torch.int32, device=dev),
+               bonus=torch.empty(B, dtype=torch.int32, device=dev))
+    L = ts.library()
+    ws = torch.empty(max(256, L.ts_tree_accept_sample_workspace(B, V, 1)), dtype=torch.uint8, device=dev)
+    elt = logits.element_size()
+    res = {"temperature": temperature, "input": "step logits, one child per expanded node raised to ln(V)+U(0,4)"}
+    for mode in ("point", "draft"):
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ts.tree_accept_sample(logits, tok, par, uniforms, temperature, q_mode=mode, draft_logp=d["draft_logp"],
+                                  node_row=nrow, out=out, workspace=ws, status=step.status)
+            b_.record(stream)
+            if i >= args.warmup:
+                times.append((a, b_))
+        torch.cuda.synchronize()
+        ts.check_status(step.status)
+        ms = sum(a.elapsed_time(b_) for a, b_ in times) / len(times)
+        alen = out["accept_len"].cpu().numpy()
+        # one read of every visited node's target row, one more of the last node's (the draw);
+        # draft mode also reads the draft row of every visited node that has children
+        byts = int(sum(int(a_) + 1 for a_ in alen) * V * elt)
+        if mode == "draft":
+            path = out["accept_path"].cpu().numpy()
+            has = [set(par_h[b][par_h[b] >= 0].tolist()) for b in range(B)]
+            byts += int(sum(1 for b in range(B) for j in range(alen[b]) if path[b, j] in has[b]) * V * 4)
+        r = {"ms": round(ms, 5), "mean_accept_len": round(float(alen.mean()), 3),
+             "bytes_min": byts, "gb_s": round(byts / (ms * 1e-3) / 1e9, 1),
+             "bound": "latency (one CTA per sequence walks the tree; a few row passes per level)"}
+        if not args.no_cpu_baseline and world == 1:
+            import oracle
+            lh = logits.float().cpu().numpy()
+            dh = d["draft_logp"].cpu().numpy() if mode == "draft" else None
+            t0 = time.perf_counter()
+            ref = oracle.accept_sample(lh, tok_h, par_h, uniforms.cpu().numpy(), temperature, mode, dh,
+                                       nrow.cpu().numpy())
+            r["oracle_ms"] = round((time.perf_counter() - t0) * 1e3, 2)
+            r["oracle_same_len"] = float((ref[0] == alen).mean())
+        res[mode] = r
+    del logits
+    return res
 
 
 def run_kv_commit(step, w, args, flush, stream, world):
