@@ -543,6 +543,640 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs a)
   for (int i = tid; i < m; i += kThreads) a.accept_path[bm + i] = i < s_plen ? s_path[i] : -1;
 }
 
+// =====================================================================================
+// Cluster path (V <= kClusterMaxVocab): one thread-block cluster of C <= 8 CTAs per
+// sequence.  CTA r owns the vocabulary slice [r*NT*EPT, (r+1)*NT*EPT); every thread keeps EPT
+// of its ids in registers (chunk j covers NT*VEC consecutive ids, thread t its VEC ids at
+// offset t*VEC), so a node's target row (and draft row) is read from HBM once and every
+// residual update, sum and the inverse CDF run on registers.  Cluster-wide values go through
+// a small exchange record per CTA read over distributed shared memory.  Every CTA takes every
+// decision itself from the same data in the same order, so the CTAs stay in lockstep
+// without broadcasts and execute the same cluster barriers.
+// =====================================================================================
+namespace cl {
+
+constexpr int NT = 512;
+constexpr int NW = NT / kWarp;
+constexpr int CMAX = 8;
+constexpr int EPT_MAX = 32;
+
+// One CTA's share of a cluster exchange (two buffers, alternated: one cluster barrier per
+// exchange suffices, since a CTA rewrites a buffer only after every CTA has passed the
+// barrier that follows its last read of it).
+struct __align__(16) Xch {
+  float M, S;      // node start: target slice (max of scaled logits, sum of 2^(s - max))
+  float Mq, Sq;    // node start, draft mode: the same for the draft slice (log2 units)
+  float w, q;      // residual step: sum of the new residual, remaining proposal mass
+  float pnext, wnext;  // residual step: current / new residual at the next child (owner only)
+  double tot;      // final draw: mass of the slice
+  double pad;
+};
+
+__device__ __forceinline__ double ld_peer_f64(uint32_t local, uint32_t rank) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(dsmem_addr(local, rank)) : "memory");
+  return v;
+}
+
+// Warp 0: lane r < C fetches 16 bytes of rank r's exchange record (one load per lane, all in
+// flight together).  The merges below reduce over the lanes in a fixed butterfly order, the
+// same in every CTA of the cluster.
+__device__ __forceinline__ float4 fetch4(uint32_t local, int C, float4 dflt) {
+  const int lane = threadIdx.x & 31;
+  return lane < C ? ld_dsmem_f4(dsmem_addr(local, lane)) : dflt;
+}
+__device__ __forceinline__ float warp_max_f(float x) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+  return x;
+}
+__device__ __forceinline__ float warp_sum_f(float x) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+  return x;
+}
+
+// Whether id x lies in this thread's registers, and in which.
+template <int VEC, int EPT>
+__device__ __forceinline__ bool owns(long long x, long long slice0, int tid, int& reg) {
+  const long long off = x - slice0;
+  if (off < 0 || off >= static_cast<long long>(NT) * EPT) return false;
+  const int o = static_cast<int>(off);
+  const int rem = o % (NT * VEC);
+  if (rem / VEC != tid) return false;
+  reg = (o / (NT * VEC)) * VEC + rem % VEC;
+  return true;
+}
+
+// Block max and sum of 2^(s - max) over this thread's values; valid in thread 0 only.
+template <int EPT>
+__device__ __forceinline__ float2 block_max_sum_t0(const float (&s)[EPT], float* red) {
+  __syncthreads();  // thread 0 may still be reading red[] from the previous reduction
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) M = fmaxf(M, s[i]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  float Mc = red[0];
+  for (int w = 1; w < NW; ++w) Mc = fmaxf(Mc, red[w]);
+  float S = 0.f;
+  if (Mc != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) S += mass(s[i], Mc);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) S += __shfl_xor_sync(kFull, S, off);
+  __syncthreads();  // every thread has read red[] before it is overwritten
+  if (lane == 0) red[warp] = S;
+  __syncthreads();
+  float St = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < NW; ++w) St += red[w];
+  return make_float2(Mc, St);
+}
+
+// Block sums of four floats in a fixed order; the result is valid in thread 0 only.
+__device__ __forceinline__ float4 block_sum4_t0(float a, float b, float c, float d, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();  // thread 0 may still be reading red[] from the previous reduction
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    a += __shfl_xor_sync(kFull, a, off);
+    b += __shfl_xor_sync(kFull, b, off);
+    c += __shfl_xor_sync(kFull, c, off);
+    d += __shfl_xor_sync(kFull, d, off);
+  }
+  if (lane == 0) red[warp] = a, red[NW + warp] = b, red[2 * NW + warp] = c, red[3 * NW + warp] = d;
+  __syncthreads();
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (threadIdx.x == 0)
+    for (int w = 0; w < NW; ++w) r.x += red[w], r.y += red[NW + w], r.z += red[2 * NW + w], r.w += red[3 * NW + w];
+  return r;
+}
+
+__device__ __forceinline__ double warp_incl_scan_f64(double x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double y = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
+}
+
+// Float-float sums for the inverse CDF: (hi, lo) with hi + lo the running sum.  Each addition
+// is an exact two-sum (the rounding error of hi + b is recovered in full), so the pair keeps
+// about 44 bits; the fp32 pipe is used because this GPU's fp64 rate is a small fraction of
+// its fp32 rate.  The two-sum is symmetric in its operands, so the butterfly reductions give
+// every lane the same pair.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = df_two_sum(a.hi, b.hi);
+  const float lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s.hi, lo);
+  return {hi, __fsub_rn(lo, __fsub_rn(hi, s.hi))};
+}
+__device__ __forceinline__ DF df_add1(DF a, float b) { return df_add(a, DF{b, 0.f}); }
+__device__ __forceinline__ double df_to_d(DF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+__device__ __forceinline__ DF df_shfl(DF a, int src) {
+  return {__shfl_sync(kFull, a.hi, src), __shfl_sync(kFull, a.lo, src)};
+}
+__device__ __forceinline__ DF df_warp_sum(DF a) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) a = df_add(a, DF{__shfl_xor_sync(kFull, a.hi, off), __shfl_xor_sync(kFull, a.lo, off)});
+  return a;
+}
+__device__ __forceinline__ DF df_warp_incl_scan(DF a) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const DF y{__shfl_up_sync(kFull, a.hi, off), __shfl_up_sync(kFull, a.lo, off)};
+    if (lane >= off) a = df_add(a, y);
+  }
+  return a;
+}
+__device__ __forceinline__ DF df_warp_excl(DF inc) {
+  DF e{__shfl_up_sync(kFull, inc.hi, 1), __shfl_up_sync(kFull, inc.lo, 1)};
+  if ((threadIdx.x & 31) == 0) e = DF{0.f, 0.f};
+  return e;
+}
+
+struct State {        // the walk's state, written by thread 0 of every CTA (identical values)
+  float M, invZ;      // target row: max of the scaled logits, 1 / total mass
+  float Mq, invZq;    // draft row: max (log2 units), 1 / remaining proposal mass (0 if none)
+  float pinv;         // p = pv * pinv (pv: registers; the target masses, later the residual)
+  float pnext;        // draft mode: p at the next child after a residual step
+  int u, plen, nk, acc, nrej, apply, sel, chunk, retry;
+  double tl, tc;      // final draw: target within the selected slice / chunk
+};
+
+}  // namespace cl
+
+template <typename T, int VEC, int EPT>
+__global__ void __launch_bounds__(cl::NT, 1) sample_cluster_kernel(const SampleArgs a, int C) {
+  using namespace cl;
+  constexpr int NCH = EPT / VEC;  // chunks per thread
+  __shared__ int s_par[TS_MAX_NODES], s_tok[TS_MAX_NODES], s_nrow[TS_MAX_NODES], s_path[TS_MAX_NODES];
+  __shared__ int s_kid[TS_MAX_NODES], s_kx[TS_MAX_NODES], s_rej[TS_MAX_NODES];
+  __shared__ float s_kr[TS_MAX_NODES], s_ks[TS_MAX_NODES], s_kd[TS_MAX_NODES];
+  __shared__ unsigned char s_has[TS_MAX_NODES];
+  __shared__ float s_red[4 * NW];
+  __shared__ DF s_dred[NW * NCH];
+  __shared__ double s_ct[NCH], s_cpre[NCH];
+  __shared__ Xch s_x[2];
+  __shared__ State st;
+  __shared__ int s_y, s_last;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int b = blockIdx.x / C;
+  const int m = a.m, V = a.V;
+  const long long bm = static_cast<long long>(b) * m;
+  const long long slice0 = static_cast<long long>(rank) * NT * EPT;
+  pdl_wait();
+
+  // ---- load and check the tree: every CTA of the cluster reads the same data and takes
+  //      the same exit, before any cluster barrier ------------------------------------------
+  for (int i = tid; i < m; i += NT) s_has[i] = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int i = tid; i < m; i += NT) {
+    const int p = a.parents[bm + i], t = a.tokens[bm + i];
+    s_par[i] = p;
+    s_tok[i] = t;
+    if (i == 0 ? p != -1 : (p < 0 || p >= i || t < 0 || t >= V)) bad = 1;
+    else if (i > 0) s_has[p] = 1;
+  }
+  __syncthreads();
+  if (a.q_draft) {
+    for (int i = tid; i < m; i += NT) {
+      const int r = a.node_row[bm + i];
+      s_nrow[i] = r;
+      if (s_has[i] && (r < 0 || r >= a.R)) bad = 1;
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (rank == 0) {
+      if (tid == 0) {
+        report(a.dev_status, TS_ERR_DEVICE_CHECK);
+        a.accept_len[b] = 0;
+        a.bonus[b] = -1;
+      }
+      for (int i = tid; i < m; i += NT) a.accept_path[bm + i] = -1;
+    }
+    return;
+  }
+
+  const T* logits = static_cast<const T*>(a.logits);
+  if (tid == 0) st.u = 0, st.plen = 1, s_path[0] = 0;
+  __syncthreads();
+  int xb = 0;          // exchange buffer
+  float pv[EPT], qv[EPT];
+
+  for (;;) {
+    const int u = st.u;
+    const T* row = logits + (bm + u) * static_cast<long long>(V);
+    const bool draft = a.q_draft && s_has[u];
+    const float* drow =
+        draft ? a.draft_logp + (static_cast<long long>(b) * a.R + s_nrow[u]) * static_cast<long long>(V) : nullptr;
+
+    // children of u in flat order; the first 32 children's tokens, uniforms and logits are
+    // fetched before the slice loads and stored after them
+    int nk = 0, px = 0;
+    float pr = 0.f, pl = 0.f, pd = 0.f;
+    if (warp == 0) {
+      for (int base = 0; base < m; base += 32) {
+        const int c = base + lane;
+        const bool is = c < m && s_par[c] == u;
+        const unsigned bal = __ballot_sync(kFull, is);
+        if (is) s_kid[nk + __popc(bal & ((1u << lane) - 1u))] = c;
+        nk += __popc(bal);
+      }
+      __syncwarp();
+      if (lane < nk) {
+        const int c = s_kid[lane];
+        px = s_tok[c];
+        pr = a.uniforms[bm + c];
+        float lx[1];
+        load_vec<1>(row, px, lx);
+        pl = lx[0];
+        if (drow) pd = __ldg(drow + px);
+      }
+    }
+
+    // this CTA's slice of the target row (scaled logits) and of the draft row (log2 units)
+#pragma unroll
+    for (int jc = 0; jc < NCH; ++jc) {
+      const long long i0 = slice0 + (static_cast<long long>(jc) * NT + tid) * VEC;
+      float v[VEC];
+      if (i0 < V) {
+        load_vec<VEC>(row, i0, v);
+      } else {
+#pragma unroll
+        for (int t = 0; t < VEC; ++t) v[t] = -INFINITY;
+      }
+#pragma unroll
+      for (int t = 0; t < VEC; ++t) pv[jc * VEC + t] = __fmul_rn(v[t], a.c);
+    }
+    if (drow) {
+#pragma unroll
+      for (int jc = 0; jc < NCH; ++jc) {
+        const long long i0 = slice0 + (static_cast<long long>(jc) * NT + tid) * VEC;
+        float v[VEC];
+        if (i0 < V) {
+          load_vec<VEC>(drow, i0, v);
+        } else {
+#pragma unroll
+          for (int t = 0; t < VEC; ++t) v[t] = -INFINITY;
+        }
+#pragma unroll
+        for (int t = 0; t < VEC; ++t) qv[jc * VEC + t] = __fmul_rn(v[t], kLog2e);
+      }
+    }
+    if (warp == 0) {
+      if (lane < nk) {
+        s_kx[lane] = px;
+        s_kr[lane] = pr;
+        s_ks[lane] = __fmul_rn(pl, a.c);
+        s_kd[lane] = __fmul_rn(pd, kLog2e);
+      }
+      for (int j = 32 + lane; j < nk; j += 32) {
+        const int c = s_kid[j], x = s_tok[c];
+        s_kx[j] = x;
+        s_kr[j] = a.uniforms[bm + c];
+        float lx[1];
+        load_vec<1>(row, x, lx);
+        s_ks[j] = __fmul_rn(lx[0], a.c);
+        s_kd[j] = drow ? __fmul_rn(__ldg(drow + x), kLog2e) : 0.f;
+      }
+      if (lane == 0) st.nk = nk;
+    }
+
+    // node start: (max, sum) of the slices, merged over the cluster in rank order
+    const float2 t2 = block_max_sum_t0<EPT>(pv, s_red);
+    float2 q2 = make_float2(-INFINITY, 0.f);
+    if (drow) q2 = block_max_sum_t0<EPT>(qv, s_red);
+    if (tid == 0) s_x[xb].M = t2.x, s_x[xb].S = t2.y, s_x[xb].Mq = q2.x, s_x[xb].Sq = q2.y;
+    cluster_sync_all();
+    float M = 0.f, Z = 0.f, Mq = 0.f, Zq = 0.f;
+    if (warp == 0) {
+      const float4 f = fetch4(smem_u32(&s_x[xb]) + offsetof(Xch, M), C, make_float4(-INFINITY, 0.f, -INFINITY, 0.f));
+      M = warp_max_f(f.x);
+      Mq = warp_max_f(f.z);
+      Z = warp_sum_f(f.x != -INFINITY ? f.y * ex2_approx(f.x - M) : 0.f);
+      Zq = warp_sum_f(f.z != -INFINITY ? f.w * ex2_approx(f.z - Mq) : 0.f);
+    }
+    if (tid == 0) {
+      st.M = M;
+      st.invZ = 1.f / Z;
+      st.Mq = Mq;
+      st.invZq = Zq > 0.f ? 1.f / Zq : 0.f;
+      st.pinv = st.invZ;
+      st.acc = -1;
+      st.nrej = 0;
+    }
+    if (warp == 0 && !a.q_draft) {
+      // Point proposals: child j is kept iff r_j * Z_left(j) < e(x_j), Z_left(j) = Z minus the
+      // mass of the distinct tokens rejected before it.  Lane j takes child j (32 at a time):
+      // a prefix sum gives Z_left, a ballot the first kept child; a token repeated among the
+      // siblings has no mass left after its first trial.
+      const int nk_ = st.nk;
+      float base = 0.f;
+      int acc = -1, nrej = 0;
+      for (int g0 = 0; g0 < nk_ && acc < 0; g0 += 32) {
+        const int j = g0 + lane;
+        const bool valid = j < nk_;
+        const int x = valid ? s_kx[j] : -1 - lane;
+        bool dup = (__match_any_sync(kFull, x) & ((1u << lane) - 1u)) != 0;
+        if (valid && !dup)
+          for (int r = 0; r < nrej; ++r) dup |= s_rej[r] == x;
+        const float e = (valid && !dup) ? mass(s_ks[j], M) : 0.f;
+        const float inc = warp_incl_scan(e);
+        float exc = __shfl_up_sync(kFull, inc, 1);
+        if (lane == 0) exc = 0.f;
+        const float Zl = __fsub_rn(Z, __fadd_rn(base, exc));
+        const unsigned kb = __ballot_sync(kFull, valid && s_kr[j] * Zl < e);
+        const int first = kb ? __ffs(kb) - 1 : 32;
+        const bool rej = valid && !dup && lane < first;
+        const unsigned rb = __ballot_sync(kFull, rej);
+        __syncwarp();
+        if (rej) s_rej[nrej + __popc(rb & ((1u << lane) - 1u))] = x;
+        __syncwarp();
+        nrej += __popc(rb);
+        base = __fadd_rn(base, __shfl_sync(kFull, inc, 31));
+        if (kb) acc = g0 + first;
+      }
+      if (lane == 0) st.acc = acc, st.nrej = nrej;
+    }
+    xb ^= 1;
+    __syncthreads();
+    // masses in registers: pv = 2^(s - M) (p = pv / Z), qv = 2^(d - Mq)
+    {
+      const float M = st.M;
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) pv[i] = mass(pv[i], M);
+      if (drow) {
+        const float Mq = st.Mq;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) qv[i] = mass(qv[i], Mq);
+      }
+    }
+
+    if (draft) {  // draft proposals: one trial at a time, one residual step per rejection
+      for (int j = 0; j < st.nk; ++j) {
+        if (tid == 0) {
+          const int x = s_kx[j];
+          bool in = false;
+          for (int r = 0; r < st.nrej; ++r) in |= s_rej[r] == x;
+          const float p = j == 0 ? mass(s_ks[0], st.M) * st.invZ : st.pnext;
+          const float q = in ? 0.f : mass(s_kd[j], st.Mq) * st.invZq;
+          st.acc = s_kr[j] * q < p ? j : -1;
+        }
+        __syncthreads();
+        if (st.acc >= 0) break;
+        // rejected x: w = max(0, p - q) on the registers; x leaves the proposal
+        const int x = s_kx[j];
+        const bool has_next = j + 1 < st.nk;
+        int rx = -1, rn = -1;
+        const bool own_x = owns<VEC, EPT>(x, slice0, tid, rx);
+        const bool own_n = has_next && owns<VEC, EPT>(s_kx[j + 1], slice0, tid, rn);
+        const float pinv = st.pinv, invZq = st.invZq;
+        float sw = 0.f, sq = 0.f, pn = 0.f, wn = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          const float p = pv[i] * pinv;
+          const float w = fmaxf(0.f, p - qv[i] * invZq);
+          sw += w;
+          if (!(own_x && i == rx)) sq += qv[i];
+          if (own_n && i == rn) pn = p, wn = w;
+        }
+        const float4 r4 = block_sum4_t0(sw, sq, pn, wn, s_red);
+        if (tid == 0) s_x[xb].w = r4.x, s_x[xb].q = r4.y, s_x[xb].pnext = r4.z, s_x[xb].wnext = r4.w;
+        cluster_sync_all();
+        float tw = 0.f, tq = 0.f, tp = 0.f, tn = 0.f;
+        if (warp == 0) {
+          const float4 f = fetch4(smem_u32(&s_x[xb]) + offsetof(Xch, w), C, make_float4(0.f, 0.f, 0.f, 0.f));
+          tw = warp_sum_f(f.x);
+          tq = warp_sum_f(f.y);
+          tp = warp_sum_f(f.z);
+          tn = warp_sum_f(f.w);
+        }
+        if (tid == 0) {
+          st.apply = tw > 0.f;  // a residual of zero mass leaves p as it was
+          if (tw > 0.f) {
+            st.pinv = 1.f / tw;
+            st.pnext = tn / tw;
+          } else {
+            st.pnext = tp;
+          }
+          st.invZq = tq > 0.f ? 1.f / tq : 0.f;
+          bool in = false;
+          for (int r = 0; r < st.nrej; ++r) in |= s_rej[r] == x;
+          if (!in) s_rej[st.nrej++] = x;
+        }
+        xb ^= 1;
+        __syncthreads();
+        if (st.apply) {
+#pragma unroll
+          for (int i = 0; i < EPT; ++i) pv[i] = fmaxf(0.f, pv[i] * pinv - qv[i] * invZq);
+        }
+        if (own_x) {
+#pragma unroll
+          for (int i = 0; i < EPT; ++i)
+            if (i == rx) qv[i] = 0.f;
+        }
+      }
+    }
+
+    if (st.acc >= 0) {  // walk down to the kept child
+      __syncthreads();
+      if (tid == 0) {
+        const int c = s_kid[st.acc];
+        s_path[st.plen++] = c;
+        st.u = c;
+      }
+      __syncthreads();
+      continue;
+    }
+    break;
+  }
+
+  // ---- final draw: inverse CDF over the residual of the last node ----------------------------
+  // Chunk, slice and prefix sums are float-float pairs; slices are merged in rank order.
+  uint32_t ex = 0;  // point mode: this thread's registers holding tokens rejected at this node
+  if (!a.q_draft) {
+    for (int r = 0; r < st.nrej; ++r) {
+      int reg;
+      if (owns<VEC, EPT>(s_rej[r], slice0, tid, reg)) ex |= 1u << reg;
+    }
+  }
+  bool use_excl = true;
+  for (;;) {
+#pragma unroll
+    for (int jc = 0; jc < NCH; ++jc) {
+      DF cs{0.f, 0.f};
+#pragma unroll
+      for (int t = 0; t < VEC; ++t) {
+        const int i = jc * VEC + t;
+        cs = df_add1(cs, (use_excl && ((ex >> i) & 1u)) ? 0.f : pv[i]);
+      }
+      cs = df_warp_sum(cs);
+      if (lane == 0) s_dred[warp * NCH + jc] = cs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      DF ct{0.f, 0.f};
+      if (lane < NCH)
+        for (int w = 0; w < NW; ++w) ct = df_add(ct, s_dred[w * NCH + lane]);
+      const DF inc = df_warp_incl_scan(ct);
+      const DF exc = df_warp_excl(inc);
+      if (lane < NCH) s_ct[lane] = df_to_d(ct), s_cpre[lane] = df_to_d(exc);
+      const DF tot = df_shfl(inc, NCH - 1);
+      if (lane == 0) s_x[xb].tot = df_to_d(tot);
+    }
+    cluster_sync_all();
+    if (warp == 0) {  // slice totals over the cluster: fp64 scan over the ranks, then a ballot
+      double f = 0.0;
+      if (lane < C) f = ld_peer_f64(smem_u32(&s_x[xb]) + offsetof(Xch, tot), lane);
+      const double inc = warp_incl_scan_f64(f);
+      double exc = __shfl_up_sync(kFull, inc, 1);
+      if (lane == 0) exc = 0.0;
+      const double total = __shfl_sync(kFull, inc, 31);
+      if (lane == 0) st.retry = 0, st.sel = -1;
+      if (!(total > 0.0)) {
+        if (lane == 0) st.retry = use_excl && !a.q_draft;  // no mass left: draw from p itself
+      } else {
+        double t = static_cast<double>(a.uniforms[bm]) * total;
+        if (!(t < total)) t = __longlong_as_double(__double_as_longlong(total) - 1);
+        // the first slice whose upper bound passes t, else the last one with mass
+        const bool has = lane < C && f > 0.0;
+        const unsigned hp = __ballot_sync(kFull, has && inc > t), hh = __ballot_sync(kFull, has);
+        const int sel = hp ? __ffs(hp) - 1 : 31 - __clz(hh);
+        const double pre_sel = __shfl_sync(kFull, exc, sel);
+        if (lane == 0) st.sel = sel, st.tl = t - pre_sel;
+      }
+    }
+    xb ^= 1;
+    __syncthreads();
+    if (!st.retry) break;
+    use_excl = false;
+  }
+
+  if (static_cast<int>(rank) == st.sel) {  // this CTA's slice holds the draw
+    if (tid == 0) s_y = 0x7fffffff, s_last = -1;
+    if (warp == 0) {
+      const double tl = st.tl;
+      const bool has = lane < NCH && s_ct[lane] > 0.0;
+      const bool pass = has && s_cpre[lane] + s_ct[lane] > tl;
+      const unsigned hp = __ballot_sync(kFull, pass), hh = __ballot_sync(kFull, has);
+      const int ch = hp ? __ffs(hp) - 1 : (hh ? 31 - __clz(hh) : 0);
+      if (lane == 0) st.chunk = ch, st.tc = tl - s_cpre[ch];
+    }
+    __syncthreads();
+    const int ch = st.chunk;
+    const double tc = st.tc;
+    const long long id0 = slice0 + (static_cast<long long>(ch) * NT + tid) * VEC;
+    float v[VEC];
+#pragma unroll
+    for (int t = 0; t < VEC; ++t) v[t] = 0.f;
+#pragma unroll
+    for (int jc = 0; jc < NCH; ++jc) {
+      if (jc == ch) {
+#pragma unroll
+        for (int t = 0; t < VEC; ++t) {
+          const int i = jc * VEC + t;
+          v[t] = (use_excl && ((ex >> i) & 1u)) ? 0.f : pv[i];
+        }
+      }
+    }
+    DF mine{0.f, 0.f};
+    int lastnz = -1;
+#pragma unroll
+    for (int t = 0; t < VEC; ++t) {
+      mine = df_add1(mine, v[t]);
+      if (v[t] > 0.f) lastnz = static_cast<int>(id0 + t);
+    }
+    const DF inc = df_warp_incl_scan(mine);
+    const DF exc = df_warp_excl(inc);
+    if (lane == 31) s_dred[warp] = inc;
+    __syncthreads();
+    DF pre{0.f, 0.f};
+    for (int w = 0; w < warp; ++w) pre = df_add(pre, s_dred[w]);
+    pre = df_add(pre, exc);
+    if (lastnz >= 0) atomicMax(&s_last, lastnz);
+    if (lastnz >= 0 && df_to_d(pre) <= tc && df_to_d(df_add(pre, mine)) > tc) {
+      DF acc = pre;
+      int y = -1;
+#pragma unroll
+      for (int t = 0; t < VEC; ++t) {
+        acc = df_add1(acc, v[t]);
+        if (y < 0 && df_to_d(acc) > tc) y = static_cast<int>(id0 + t);
+      }
+      atomicMin(&s_y, y >= 0 ? y : lastnz);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int y = s_y != 0x7fffffff ? s_y : s_last;
+      a.bonus[b] = y;
+      if (y < 0) report(a.dev_status, TS_ERR_DEVICE_CHECK);
+    }
+  }
+  if (rank == 0) {
+    if (tid == 0) {
+      a.accept_len[b] = st.plen;
+      if (st.sel < 0) {  // the target row had no mass
+        a.bonus[b] = -1;
+        report(a.dev_status, TS_ERR_DEVICE_CHECK);
+      }
+    }
+    for (int i = tid; i < m; i += NT) a.accept_path[bm + i] = i < st.plen ? s_path[i] : -1;
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still read its exchange record
+}
+
+template <typename T, int VEC, int EPT>
+int launch_cluster(const SampleArgs& a, int B, int C, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * C);
+  cfg.blockDim = dim3(cl::NT);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, sample_cluster_kernel<T, VEC, EPT>, a, C) != cudaSuccess) return TS_ERR_CUDA;
+  count_launches(1);
+  return TS_OK;
+}
+
+// Registers per thread and cluster size for a vocabulary: the smallest EPT whose cluster of
+// at most CMAX CTAs covers V.
+template <typename T, int VEC>
+int dispatch_cluster(const SampleArgs& a, int B, cudaStream_t stream) {
+  const int V = a.V;
+  if (V <= cl::CMAX * cl::NT * 8) return launch_cluster<T, VEC, 8>(a, B, (V + cl::NT * 8 - 1) / (cl::NT * 8), stream);
+  if (V <= cl::CMAX * cl::NT * 16)
+    return launch_cluster<T, VEC, 16>(a, B, (V + cl::NT * 16 - 1) / (cl::NT * 16), stream);
+  return launch_cluster<T, VEC, 32>(a, B, (V + cl::NT * 32 - 1) / (cl::NT * 32), stream);
+}
+
+
 template <typename T, int VEC>
 int launch_one(const SampleArgs& a, int B, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>((a.V + 31) / 32) * 4;
@@ -596,6 +1230,14 @@ int tree_accept_sample_launch(const void* logits, ts_dtype dt, const int32_t* to
   a.dev_status = dev_status;
   const bool al = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 &&
                   (!a.q_draft || (reinterpret_cast<uintptr_t>(draft_logp) & 15) == 0);
+  if (V <= cl::CMAX * cl::NT * cl::EPT_MAX) {  // the row fits the registers of one cluster
+    if (dt == TS_BF16) {
+      if (al && V % 8 == 0) return dispatch_cluster<__nv_bfloat16, 8>(a, B, stream);
+      return dispatch_cluster<__nv_bfloat16, 1>(a, B, stream);
+    }
+    if (al && V % 4 == 0) return dispatch_cluster<float, 4>(a, B, stream);
+    return dispatch_cluster<float, 1>(a, B, stream);
+  }
   if (dt == TS_BF16) {
     if (al && V % 8 == 0) return launch_one<__nv_bfloat16, 8>(a, B, stream);
     return launch_one<__nv_bfloat16, 1>(a, B, stream);

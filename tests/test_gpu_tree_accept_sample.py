@@ -103,7 +103,8 @@ CASES = [dict(dt=torch.float32, B=16, m=40, V=1000, T=1.0),
          dict(dt=torch.float32, B=4, m=33, V=4097, T=1.3),           # V odd: scalar loads
          dict(dt=torch.bfloat16, B=8, m=64, V=128256, T=1.0),
          dict(dt=torch.bfloat16, B=3, m=256, V=2000, T=1.0),          # largest tree
-         dict(dt=torch.bfloat16, B=2, m=20, V=1003, T=2.0)]           # bf16, V % 8 != 0
+         dict(dt=torch.bfloat16, B=2, m=20, V=1003, T=2.0),           # bf16, V % 8 != 0
+         dict(dt=torch.bfloat16, B=8, m=24, V=140000, T=1.0)]         # beyond one cluster: streaming kernel
 
 
 @pytest.mark.parametrize("mode", ["point", "draft"])
