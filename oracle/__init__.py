@@ -15,6 +15,10 @@ Plain, slow, obviously-correct numpy restatements of what the pages define:
   EAGLE-4 efficient LM head", local Top-k section; "lesty.tech", section 4).
 * :mod:`oracle.efficient_head` — the draft's two-stage efficient LM head (low-rank scores,
   local top-k per vocabulary tile, exact logits of the candidates; same page).
+* :mod:`oracle.accept_sample` — verification at T > 0 by multi-round rejection sampling
+  ("lesty.tech", section 4).
+* :mod:`oracle.tree_prune`   — cost-aware pruning of the tree before verification (same
+  page, EAGLE-Harness section; "rainlin.net/posts/eagle", sections 7.1 and 六).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
@@ -31,3 +35,4 @@ from .kv_commit import kv_commit  # noqa: F401
 from .lm_head import lm_head_logits, lm_head_argmax, fp32_error_bound  # noqa: F401
 from .efficient_head import candidates, efficient_head  # noqa: F401
 from .accept_sample import accept_sample, softmax_t  # noqa: F401
+from .tree_prune import tree_prune  # noqa: F401
