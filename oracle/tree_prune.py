@@ -54,8 +54,10 @@ def expected_tokens(values, order, n: int) -> float:
     return 1.0 + float(sum(np.exp(float(values[i])) for i in order[: n - 1]))
 
 
-def tree_prune(tokens, parents, depth, values, t_draft: float, t_fixed: float, t_node: float, node_row=None):
-    """Batched pruning.  ``values`` fp64 [B, m] (from tree_build, flat order).
+def tree_prune(tokens, parents, depth, values, t_draft: float, t_fixed: float, t_node: float, node_row=None,
+               n=None):
+    """Batched pruning.  ``values`` fp64 [B, m] (from tree_build, flat order).  ``n`` forces
+    the kept node count (the rates are still returned).
 
     Returns (n, out, rate) with n the kept node count (root included), ``rate`` fp64 [m] the
     rate of every candidate n = 1..m, and ``out`` holding int64 ``tokens``, ``parents``,
@@ -66,10 +68,10 @@ def tree_prune(tokens, parents, depth, values, t_draft: float, t_fixed: float, t
     B, m = values.shape
     orders = [rerank_order(values[b], depth[b]) for b in range(B)]
     rate = np.zeros(m)
-    for n in range(1, m + 1):
-        tok = sum(expected_tokens(values[b], orders[b], n) for b in range(B))
-        rate[n - 1] = tok / (t_draft + t_fixed + t_node * B * n)
-    best = int(np.argmax(rate)) + 1            # first maximum: ties -> smaller n
+    for c in range(1, m + 1):
+        tok = sum(expected_tokens(values[b], orders[b], c) for b in range(B))
+        rate[c - 1] = tok / (t_draft + t_fixed + t_node * B * c)
+    best = int(np.argmax(rate)) + 1 if n is None else int(n)   # first maximum: ties -> smaller n
     out = {k: np.zeros((B, best), dtype=np.int64) for k in ("tokens", "parents", "depth", "kept")}
     if node_row is not None:
         out["node_row"] = np.zeros((B, best), dtype=np.int64)
