@@ -7,6 +7,7 @@
  *   ts_tree_attention  every tree node attends to the paged KV prefix + its own ancestors
  *   ts_tree_accept     per-node argmax of the target logits + longest matching root path
  *   ts_tree_accept_sample  the same verification at temperature T > 0 (rejection sampling)
+ *   ts_tree_prune      cost-aware pruning of the tree before verification
  *
  * Conventions shared by every entry point
  *   - Every tensor argument is a DEVICE pointer owned by the caller.  The library never
@@ -371,6 +372,41 @@ int ts_tree_accept_sample(const void* logits, ts_dtype dt, const int32_t* tokens
                           int B, int m, int V, float temperature, int q_mode, int32_t* accept_len,
                           int32_t* accept_path, int32_t* bonus, void* workspace, size_t ws_bytes,
                           int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * ts_tree_prune — cost-aware pruning of the draft tree before verification.
+ * Sources: "jialefu.github.io — EAGLE-4 efficient LM head", section EAGLE-Harness (prune the
+ * tree from draft and target costs and the draft confidence; the page gives no formula);
+ * "rainlin.net/posts/eagle", sections 7.1 (value = product of the confidences on the root
+ * path) and 六 (the confidence tracks the acceptance rate).
+ *
+ * Expected tokens of verifying a tree: 1 + sum over its non-root nodes of exp(values).  The
+ * candidate trees are the prefixes of the rerank order (value descending, then shallower,
+ * then lower flat index), each a connected tree because values never increase along a path.
+ * One node count n (root included) is chosen for the whole batch, the first maximum over
+ * n = 1..m of
+ *     sum_b (1 + sum of exp(values) over the first n-1 nodes of b) / (t_draft + t_fixed + t_node*B*n)
+ * (t_draft: the round's drafting time; t_fixed, t_node: the verification pass's fixed and
+ * per-node time; any unit, all >= 0 with a positive sum).  exp and the sums run in fp32.
+ *
+ * tokens, parents, depth [B, m] int32 and values [B, m] double: a tree as ts_tree_build
+ *   writes it; node_row [B, m] int32 optional (NULL: node_row_out is not written).
+ * Outputs (device, capacity for n = m; written COMPACTLY with row stride n, so after
+ * reading *n_out the first B*n entries form [B, n]):
+ *   n_out [1] int32; tokens_out, parents_out, depth_out, node_row_out, kept_out (the old
+ *   flat index of each kept node) [B, n] int32; values_out [B, n] double; mask_out
+ *   [B, n, ceil(n/64)] uint64 (the ancestor mask of the pruned tree); expected_out [B] float
+ *   (1 + the kept nodes' sum of exp(values)).  Kept nodes keep their flat order.
+ * Workspace: ts_tree_prune_workspace(B, m) bytes.  Limits: m <= TS_MAX_NODES.
+ * Device errors: a parent not preceding its child, or a kept node whose parent is not kept
+ * (a value above its parent's) -> TS_ERR_DEVICE_CHECK.  Three launches, no host sync.
+ * --------------------------------------------------------------------------------- */
+size_t ts_tree_prune_workspace(int B, int m);
+int ts_tree_prune(const int32_t* tokens, const int32_t* parents, const int32_t* depth, const double* values,
+                  const int32_t* node_row, int B, int m, double t_draft, double t_fixed, double t_node,
+                  int32_t* n_out, int32_t* tokens_out, int32_t* parents_out, int32_t* depth_out,
+                  uint64_t* mask_out, double* values_out, int32_t* node_row_out, int32_t* kept_out,
+                  float* expected_out, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,11 @@ def library():
         L.ts_tree_accept_sample_workspace.argtypes = [I, I, I]
         L.ts_tree_accept_sample.restype = I
         L.ts_tree_accept_sample.argtypes = [P, I, P, P, P, P, P, I, I, I, I, F, I, P, P, P, P, S, P, P]
+        L.ts_tree_prune_workspace.restype = S
+        L.ts_tree_prune_workspace.argtypes = [I, I]
+        L.ts_tree_prune.restype = I
+        D = ctypes.c_double
+        L.ts_tree_prune.argtypes = [P, P, P, P, P, I, I, D, D, D, P, P, P, P, P, P, P, P, P, P, S, P, P]
         L.ts_kv_commit.restype = I
         L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L
@@ -320,6 +325,57 @@ def tree_accept_sample(logits: torch.Tensor, tokens: torch.Tensor, parents: torc
                                    _p(node_row), R, B, m, V, float(temperature), Q_MODES[q_mode],
                                    _p(out["accept_len"]), _p(out["accept_path"]), _p(out["bonus"]), _p(ws), nbytes,
                                    _p(status), _stream()))
+    return out
+
+
+def tree_prune(tree: Dict[str, torch.Tensor], t_draft: float, t_fixed: float, t_node: float, *,
+               workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+               sync: bool = True) -> Dict[str, torch.Tensor]:
+    """Cost-aware pruning before verification of a tree from tree_build (``tokens``, ``parents``,
+    ``depth`` int32 and ``values`` float64 [B,m]; ``node_row`` optional).  One node count n for
+    the batch maximises expected tokens per unit of round time (t_draft + t_fixed + t_node*B*n).
+    Returns ``n`` (a device int32 [1]) and the pruned tree: ``tokens``, ``parents``, ``depth``,
+    ``kept`` (old flat indices), ``node_row`` int32 and ``values`` [B,n], ``mask`` int64
+    [B,n,ceil(n/64)], ``expected`` float32 [B].  With ``sync`` (default) the host reads n and
+    the outputs are views of shape [B,n]; without it they are the flat buffers (row stride n)."""
+    L = library()
+    for name, dt in (("tokens", torch.int32), ("parents", torch.int32), ("depth", torch.int32),
+                     ("values", torch.float64)):
+        _need_cuda(name, tree[name], dt)
+    nr = tree.get("node_row")
+    if nr is not None:
+        _need_cuda("node_row", nr, torch.int32)
+    B, m = tree["tokens"].shape
+    dev = tree["tokens"].device
+    W = (m + 63) // 64
+    buf = dict(n=torch.empty(1, dtype=torch.int32, device=dev),
+               tokens=torch.empty(B * m, dtype=torch.int32, device=dev),
+               parents=torch.empty(B * m, dtype=torch.int32, device=dev),
+               depth=torch.empty(B * m, dtype=torch.int32, device=dev),
+               kept=torch.empty(B * m, dtype=torch.int32, device=dev),
+               values=torch.empty(B * m, dtype=torch.float64, device=dev),
+               mask=torch.empty(B * m * W, dtype=torch.int64, device=dev),
+               expected=torch.empty(B, dtype=torch.float32, device=dev))
+    if nr is not None:
+        buf["node_row"] = torch.empty(B * m, dtype=torch.int32, device=dev)
+    need = L.ts_tree_prune_workspace(B, m)
+    if need == 0:
+        raise TreeSpecError("invalid tree_prune sizes")
+    ws = _workspace(need, dev, workspace)
+    _check(L.ts_tree_prune(_p(tree["tokens"]), _p(tree["parents"]), _p(tree["depth"]), _p(tree["values"]), _p(nr),
+                           B, m, float(t_draft), float(t_fixed), float(t_node), _p(buf["n"]), _p(buf["tokens"]),
+                           _p(buf["parents"]), _p(buf["depth"]), _p(buf["mask"]), _p(buf["values"]),
+                           _p(buf.get("node_row")), _p(buf["kept"]), _p(buf["expected"]), _p(ws),
+                           ws.numel() * ws.element_size(), _p(status), _stream()))
+    if not sync:
+        return buf
+    n = int(buf["n"].item())
+    Wn = (n + 63) // 64
+    out = {"n": buf["n"], "expected": buf["expected"]}
+    for k in ("tokens", "parents", "depth", "kept", "values", "node_row"):
+        if k in buf:
+            out[k] = buf[k][: B * n].view(B, n)
+    out["mask"] = buf["mask"][: B * n * Wn].view(B, n, Wn)
     return out
 
 

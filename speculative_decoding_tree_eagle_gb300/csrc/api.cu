@@ -321,4 +321,29 @@ int ts_tree_accept_sample(const void* logits, ts_dtype dt, const int32_t* tokens
                                        static_cast<cudaStream_t>(stream));
 }
 
+size_t ts_tree_prune_workspace(int B, int m) {
+  if (B <= 0 || m <= 0 || m > TS_MAX_NODES) return 0;
+  return ts::tree_prune_workspace_bytes(B, m);
+}
+
+int ts_tree_prune(const int32_t* tokens, const int32_t* parents, const int32_t* depth, const double* values,
+                  const int32_t* node_row, int B, int m, double t_draft, double t_fixed, double t_node,
+                  int32_t* n_out, int32_t* tokens_out, int32_t* parents_out, int32_t* depth_out,
+                  uint64_t* mask_out, double* values_out, int32_t* node_row_out, int32_t* kept_out,
+                  float* expected_out, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (B <= 0 || m <= 0) return TS_ERR_INVALID;
+  if (m > TS_MAX_NODES || B > 65535) return TS_ERR_UNSUPPORTED;
+  if (!(t_draft >= 0.0) || !(t_fixed >= 0.0) || !(t_node >= 0.0) || !std::isfinite(t_draft) ||
+      !std::isfinite(t_fixed) || !std::isfinite(t_node) || !(t_draft + t_fixed + t_node > 0.0))
+    return TS_ERR_INVALID;
+  if (!tokens || !parents || !depth || !values || !n_out || !tokens_out || !parents_out || !depth_out || !mask_out ||
+      !values_out || !kept_out || !expected_out || !workspace)
+    return TS_ERR_INVALID;
+  if (node_row_out && !node_row) return TS_ERR_INVALID;
+  if (ws_bytes < ts::tree_prune_workspace_bytes(B, m)) return TS_ERR_WORKSPACE;
+  return ts::tree_prune_launch(tokens, parents, depth, values, node_row, B, m, t_draft, t_fixed, t_node, n_out,
+                               tokens_out, parents_out, depth_out, mask_out, values_out, node_row_out, kept_out,
+                               expected_out, workspace, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

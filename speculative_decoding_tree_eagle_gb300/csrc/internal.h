@@ -79,6 +79,14 @@ int tree_accept_sample_launch(const void* logits, ts_dtype dt, const int32_t* to
                               int32_t* accept_path, int32_t* bonus, void* workspace, int32_t* dev_status,
                               cudaStream_t stream);
 
+// Cost-aware pruning before verification (tree_prune.cu).
+size_t tree_prune_workspace_bytes(int B, int m);
+int tree_prune_launch(const int32_t* tokens, const int32_t* parents, const int32_t* depth, const double* values,
+                      const int32_t* node_row, int B, int m, double t_draft, double t_fixed, double t_node,
+                      int32_t* n_out, int32_t* tokens_out, int32_t* parents_out, int32_t* depth_out, uint64_t* mask_out,
+                      double* values_out, int32_t* node_row_out, int32_t* kept_out, float* expected_out,
+                      void* workspace, int32_t* dev_status, cudaStream_t stream);
+
 int efficient_head_candidates(int V, int tile_tokens, int k_tile);
 size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile);
 int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M, int V,

@@ -133,6 +133,26 @@ def test_tree_accept_sample_validation(lib):
     assert lib.ts_tree_accept_sample_workspace(2, 100, 7) == 0
 
 
+def _prune(lib, B=2, m=8, td=1.0, tf=1.0, tn=0.1, ptr=1, nr=None, nro=None, ws=1, wsb=1 << 20):
+    P = ptr
+    return lib.ts_tree_prune(P, P, P, P, nr, B, m, td, tf, tn, P, P, P, P, P, P, nro, P, P, ws, wsb, None, None)
+
+
+def test_tree_prune_validation(lib):
+    assert _prune(lib, B=0) == TS_ERR_INVALID
+    assert _prune(lib, m=0) == TS_ERR_INVALID
+    assert _prune(lib, m=257) == TS_ERR_UNSUPPORTED
+    assert _prune(lib, td=-1.0) == TS_ERR_INVALID
+    assert _prune(lib, tn=float("nan")) == TS_ERR_INVALID
+    assert _prune(lib, tf=float("inf")) == TS_ERR_INVALID
+    assert _prune(lib, td=0.0, tf=0.0, tn=0.0) == TS_ERR_INVALID   # no cost at all
+    assert _prune(lib, ptr=None) == TS_ERR_INVALID
+    assert _prune(lib, nro=1) == TS_ERR_INVALID                    # node_row_out without node_row
+    assert _prune(lib, wsb=16) == -3
+    assert lib.ts_tree_prune_workspace(2, 8) >= 2 * 8 * 8
+    assert lib.ts_tree_prune_workspace(2, 257) == 0
+
+
 def test_workspace_queries_are_positive_for_valid_sizes(lib):
     assert lib.ts_tree_build_workspace(8, 128256, 10, 7, 64) > 0
     assert lib.ts_tree_accept_workspace(1, 8, 64, 128256) > 0
