@@ -348,7 +348,8 @@ def run_ours(args, rank, world, dev):
     res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world),
                         "lm_head_argmax": run_lm_head(w, args, flush, stream, dev),
                         "efficient_head": run_efficient_head(w, args, flush, stream, dev),
-                        "accept_sample": run_accept_sample(step, w, args, flush, stream, world)}
+                        "accept_sample": run_accept_sample(step, w, args, flush, stream, world),
+                        "tree_prune": run_tree_prune(step, w, args, flush, stream)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(step, w, ab, args, dev, world)
     return res, w, inp
@@ -512,6 +513,34 @@ def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
         res[mode] = r
     del logits
     return res
+
+
+def run_tree_prune(step, w, args, flush, stream, costs=(1.0, 10.0, 0.05)):
+    """Cost-aware pruning of the step's tree before verification (the harness row): three
+    launches, no host sync inside the events; the cost model (t_draft, t_fixed, t_node) is an
+    illustrative one in arbitrary units."""
+    ts = step.ts
+    tree = {k: step.tree[k] for k in ("tokens", "parents", "depth", "values", "node_row")}
+    B, m = w.B, w.m
+    dev = tree["tokens"].device
+    ws = torch.empty(max(256, ts.library().ts_tree_prune_workspace(B, m)), dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        out = ts.tree_prune(tree, *costs, workspace=ws, status=step.status, sync=False)
+        b.record(stream)
+        if i >= args.warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    ts.check_status(step.status)
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    n = int(out["n"].item())
+    W = (n + 63) // 64
+    byts = B * m * (4 * 4 + 8) + B * n * (4 * 5 + 8 + 8 * W) + B * 4
+    return {"ms": round(ms, 5), "costs": list(costs), "n": n, "algorithmic_bytes": int(byts),
+            "bound": "latency (three small launches)"}
 
 
 def run_kv_commit(step, w, args, flush, stream, world):
