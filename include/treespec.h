@@ -408,6 +408,19 @@ int ts_tree_prune(const int32_t* tokens, const int32_t* parents, const int32_t* 
                   uint64_t* mask_out, double* values_out, int32_t* node_row_out, int32_t* kept_out,
                   float* expected_out, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * ts_selftest_bounded_wait — failure-detection check of the bounded pipeline waits.
+ * The pages have no counterpart; it exists so that the timeout path can be tested without
+ * faulting or hanging a GPU.  One CTA, two warps, each waiting on its own mbarrier through
+ * the same bounded wait every kernel of the library uses:
+ *   mode 0: nothing arrives.  After the wait limit (2 s) the first wait to give up raises
+ *           the CTA's abort flag and stores TS_ERR_TIMEOUT in *dev_status, the other leaves
+ *           on the flag, and the kernel returns; the context stays usable.
+ *   mode 1: both barriers are completed first; both waits succeed at once.
+ * result [2] int32 device: 1 if warp w's wait succeeded, else 0.  One launch.
+ * --------------------------------------------------------------------------------- */
+int ts_selftest_bounded_wait(int mode, int32_t* result, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

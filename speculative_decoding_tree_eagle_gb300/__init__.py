@@ -96,6 +96,8 @@ def library():
         L.ts_tree_prune.restype = I
         D = ctypes.c_double
         L.ts_tree_prune.argtypes = [P, P, P, P, P, I, I, D, D, D, P, P, P, P, P, P, P, P, P, P, S, P, P]
+        L.ts_selftest_bounded_wait.restype = I
+        L.ts_selftest_bounded_wait.argtypes = [I, P, P, P]
         L.ts_kv_commit.restype = I
         L.ts_kv_commit.argtypes = [P, P, I, I, I, I, I, P, I, P, P, P, I, I, P, P, P, P]
         _lib = L

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtreespec.so")
 SOURCES = ["api.cu", "tree_build.cu", "tree_accept.cu", "tree_attention_simt.cu", "tree_attention_tc.cu",
-           "kv_commit.cu", "lm_head.cu", "tree_sample.cu", "tree_prune.cu"]
+           "kv_commit.cu", "lm_head.cu", "tree_sample.cu", "tree_prune.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

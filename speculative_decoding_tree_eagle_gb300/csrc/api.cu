@@ -346,4 +346,9 @@ int ts_tree_prune(const int32_t* tokens, const int32_t* parents, const int32_t* 
                                expected_out, workspace, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int ts_selftest_bounded_wait(int mode, int32_t* result, int32_t* dev_status, void* stream) {
+  if ((mode != 0 && mode != 1) || !result) return TS_ERR_INVALID;
+  return ts::selftest_bounded_wait_launch(mode, result, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

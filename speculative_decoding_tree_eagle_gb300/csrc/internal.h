@@ -87,6 +87,9 @@ int tree_prune_launch(const int32_t* tokens, const int32_t* parents, const int32
                       double* values_out, int32_t* node_row_out, int32_t* kept_out, float* expected_out,
                       void* workspace, int32_t* dev_status, cudaStream_t stream);
 
+// Bounded-wait self-test (selftest.cu).
+int selftest_bounded_wait_launch(int mode, int32_t* result, int32_t* dev_status, cudaStream_t stream);
+
 int efficient_head_candidates(int V, int tile_tokens, int k_tile);
 size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile);
 int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M, int V,

@@ -149,9 +149,11 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   }
   const int nkeys = L + p.m;
   const int T = (nkeys + BN - 1) / BN;
-  // balanced chunks: chunk c covers tiles [c*T/nc, (c+1)*T/nc) of this sequence
-  const int t0 = static_cast<int>(static_cast<long long>(chunk) * T / p.nchunk);
-  const int nt = static_cast<int>(static_cast<long long>(chunk + 1) * T / p.nchunk) - t0;
+  // balanced chunks: chunk c covers tiles [ceil(c*T/nc), ceil((c+1)*T/nc)) of this sequence,
+  // so the chunks that get one tile more are the first ones and the last chunk, which holds
+  // the masked tree tile, is never the longest
+  const int t0 = static_cast<int>((static_cast<long long>(chunk) * T + p.nchunk - 1) / p.nchunk);
+  const int nt = static_cast<int>((static_cast<long long>(chunk + 1) * T + p.nchunk - 1) / p.nchunk) - t0;
   if (nt == 0 && p.mode != kCluster) return;  // (an idle CTA of a cluster still merges)
   // a sequence whose tiles all fall into one chunk is written directly also in the global mode
   const bool direct = p.mode == kDirect || (p.mode == kGlobal && min(T, p.nchunk) == 1);
@@ -629,9 +631,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int nc = p.nchunk;
   if (min(T, nc) <= 1) return;  // written directly by the attention kernel
   const long long prow = static_cast<long long>(wid) * nc;
-  // chunk c holds tiles [c*T/nc, (c+1)*T/nc); empty chunks wrote nothing
+  // chunk c holds tiles [ceil(c*T/nc), ceil((c+1)*T/nc)); empty chunks wrote nothing
   auto empty = [&](int c) {
-    return static_cast<long long>(c + 1) * T / nc == static_cast<long long>(c) * T / nc;
+    return (static_cast<long long>(c + 1) * T + nc - 1) / nc == (static_cast<long long>(c) * T + nc - 1) / nc;
   };
   float M = -INFINITY;
 #pragma unroll 4

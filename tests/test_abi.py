@@ -153,6 +153,11 @@ def test_tree_prune_validation(lib):
     assert lib.ts_tree_prune_workspace(2, 257) == 0
 
 
+def test_selftest_validation(lib):
+    assert lib.ts_selftest_bounded_wait(2, 1, None, None) == TS_ERR_INVALID
+    assert lib.ts_selftest_bounded_wait(0, None, None, None) == TS_ERR_INVALID
+
+
 def test_workspace_queries_are_positive_for_valid_sizes(lib):
     assert lib.ts_tree_build_workspace(8, 128256, 10, 7, 64) > 0
     assert lib.ts_tree_accept_workspace(1, 8, 64, 128256) > 0
