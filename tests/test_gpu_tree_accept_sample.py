@@ -290,3 +290,66 @@ def test_row_without_mass_is_reported():
     _, st = _run(lg, np.array([[0, 3]], np.int32), np.array([[-1, 0]], np.int32), np.full((1, 2), 0.5, np.float32),
                  1.0, "point", expect_ok=False)
     assert st == -6
+
+
+@pytest.mark.parametrize("mode", ["point", "draft"])
+def test_a_node_with_more_than_32_children(mode):
+    """A star-shaped level (100 children under the root, 40 under the first child): the trials
+    run in groups of 32 lanes and the children past the 32nd are fetched separately."""
+    B, V = 6, 3000
+    rng = np.random.default_rng(17)
+    par = [-1] + [0] * 100 + [1] * 40 + list(range(101, 131))
+    m = len(par)
+    parents = np.tile(np.array(par, np.int32), (B, 1))
+    tokens = np.zeros((B, m), np.int32)
+    for b in range(B):
+        for u in set(par[1:]):
+            kids = [c for c in range(m) if par[c] == u]
+            tokens[b, kids] = rng.choice(V, size=len(kids), replace=False)
+    logits = rng.normal(0, 1, size=(B, m, V)).astype(np.float32)
+    for b in range(B):                       # the kept child sits late in the sibling order
+        logits[b, 0, tokens[b, 70 + b]] = np.log(V) + 2.0
+        logits[b, 1, tokens[b, 101 + 35]] = np.log(V) + 1.0
+    uniforms = rng.random((B, m)).astype(np.float32)
+    draft = node_row = None
+    if mode == "draft":
+        draft = torch.log_softmax(torch.from_numpy(rng.normal(0, 1, size=(B, m, V)).astype(np.float32)), -1).numpy()
+        node_row = np.tile(np.arange(m, dtype=np.int32), (B, 1))
+    got, _ = _run(logits, tokens, parents, uniforms, 1.0, mode, draft, node_row)
+    ref = oracle.accept_sample(logits, tokens, parents, uniforms, 1.0, mode, draft, node_row)
+    ok = _compare(got, ref, parents, V, min_frac=0.8)
+    assert (ref[0][ok] >= 2).any()
+
+
+@pytest.mark.parametrize("V", [5, 33, 511])
+def test_tiny_vocabularies(V):
+    B, m = 8, 6
+    rng = np.random.default_rng(V)
+    parents = np.tile(np.array([-1, 0, 0, 1, 1, 2], np.int32), (B, 1))
+    tokens = np.zeros((B, m), np.int32)
+    for b in range(B):
+        tokens[b, 1:3] = rng.choice(V, size=2, replace=False)
+        tokens[b, 3:5] = rng.choice(V, size=2, replace=False)
+        tokens[b, 5] = rng.integers(V)
+    logits = rng.normal(0, 1.5, size=(B, m, V)).astype(np.float32)
+    uniforms = rng.random((B, m)).astype(np.float32)
+    for mode in ("point", "draft"):
+        draft = torch.log_softmax(torch.from_numpy(rng.normal(0, 1, size=(B, m, V)).astype(np.float32)), -1).numpy()
+        node_row = np.tile(np.arange(m, dtype=np.int32), (B, 1))
+        got, _ = _run(logits, tokens, parents, uniforms, 1.0, mode, draft if mode == "draft" else None,
+                      node_row if mode == "draft" else None)
+        ref = oracle.accept_sample(logits, tokens, parents, uniforms, 1.0, mode, draft, node_row)
+        _compare(got, ref, parents, V, min_frac=0.75)
+
+
+def test_many_sequences():
+    """300 sequences (300 clusters of 8 CTAs at V = 32000): several waves of clusters."""
+    B, m, V = 300, 12, 32000
+    rng = np.random.default_rng(5)
+    parents, tokens = _random_trees(rng, B, m, V)
+    logits = _sharpen(rng, rng.normal(0, 1, size=(B, m, V)).astype(np.float32), parents, tokens)
+    lt = torch.from_numpy(logits).to(torch.bfloat16)
+    uniforms = rng.random((B, m)).astype(np.float32)
+    got, _ = _run(lt, tokens, parents, uniforms, 1.0, "point")
+    ref = oracle.accept_sample(lt.float().numpy(), tokens, parents, uniforms, 1.0, "point")
+    _compare(got, ref, parents, V, min_frac=0.9)
