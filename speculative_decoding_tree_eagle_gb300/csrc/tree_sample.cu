@@ -9,7 +9,15 @@
 // proposals (q = a unit mass on each candidate) make a rejection simply remove the token's
 // mass from p.
 //
-// One CTA of 512 threads per sequence walks its tree.  At each visited node u:
+// Two kernels; the launcher picks by vocabulary size.
+//
+// sample_cluster_kernel (V <= 131072): one thread-block cluster of up to 8 CTAs per sequence,
+// each CTA holding its slice of the vocabulary in registers (see the cluster section below):
+// a visited node's rows are read from HBM once, draft-mode residual updates run on the
+// registers, and cluster-wide sums go through exchange records read over DSMEM.
+//
+// sample_kernel (larger vocabularies): one CTA of 512 threads per sequence streams the rows.
+// At each visited node u:
 //   pass A  one read of the target row: a per-thread running (max, sum of 2^(s - max)) with
 //           s = logit * log2(e) / T, merged across the block; in draft mode also the draft
 //           row of u (q = its exp, renormalised).  Warp 0 first lists u's children in flat
@@ -23,7 +31,7 @@
 //           contiguous segment of the residual (pieces of 32 x VEC ids, lane-ordered
 //           inclusive scans), one thread finds the segment holding r * total, and that warp
 //           rescans it with the same arithmetic to the token.
-// Rejected tokens of the current node are kept in a shared-memory bitmap over the vocabulary.
+//   Rejected tokens of the current node are kept in a shared-memory bitmap over the vocabulary.
 #include <cmath>
 #include <mutex>
 
