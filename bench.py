@@ -433,10 +433,20 @@ def run_lm_head(w, args, flush, stream, dev):
     t_hbm, t_tc = byts / (hbm * 1e9), flops / (tf * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     frac = (tb_s * 1e3 / hbm) if bound == "hbm" else (tflops / tf)
+    res = {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": K}, "algorithmic_bytes": int(byts),
+           "tb_s": round(tb_s, 4), "tflops": round(tflops, 2), "bound": bound, "frac_of_measured_peak": round(frac, 4),
+           "logits_bytes_not_written": int(M * V * 4)}
+    if not args.no_cpu_baseline and _WORLD == 1:
+        # the oracle beside it: fp64 logits and argmax of a bounded sample of rows, scaled to all rows
+        import oracle
+        n = min(M, 8)
+        hh, wh = hidden[:n].cpu(), weight.cpu()
+        t0 = time.perf_counter()
+        oracle.lm_head_argmax(hh, wh)
+        res["oracle_ms"] = round((time.perf_counter() - t0) * 1e3 * M / n, 2)
+        res["oracle_note"] = f"fp64 numpy oracle on {n} of {M} rows, scaled to all rows"
     del hidden, weight
-    return {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": K}, "algorithmic_bytes": int(byts),
-            "tb_s": round(tb_s, 4), "tflops": round(tflops, 2), "bound": bound, "frac_of_measured_peak": round(frac, 4),
-            "logits_bytes_not_written": int(M * V * 4)}
+    return res
 
 
 def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, k_tile=2):
@@ -470,11 +480,19 @@ def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, 
     C = L.ts_efficient_head_candidates(V, tile_tokens, k_tile)
     byts = (V * rank + rank * d + M * d) * 2 + M * C * d * 2 + M * k * 8
     full_head = V * d * 2
+    res = {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": d, "rank": rank, "tile_tokens": tile_tokens,
+                                         "k_tile": k_tile, "candidates": C, "k": k},
+           "algorithmic_bytes": int(byts), "tb_s": round(byts / (ms * 1e-3) / 1e12, 4),
+           "full_head_bytes": int(full_head), "bound": "hbm (low-rank head + gathered candidate rows)"}
+    if not args.no_cpu_baseline and _WORLD == 1:
+        import oracle
+        n = min(M, 2)
+        t0 = time.perf_counter()
+        oracle.efficient_head(h[:n].cpu(), B.cpu(), A.cpu(), W.cpu(), tile_tokens, k_tile, k)
+        res["oracle_ms"] = round((time.perf_counter() - t0) * 1e3 * M / n, 2)
+        res["oracle_note"] = f"fp64 numpy oracle on {n} of {M} rows, scaled to all rows"
     del h, B, A, W
-    return {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": d, "rank": rank, "tile_tokens": tile_tokens,
-                                          "k_tile": k_tile, "candidates": C, "k": k},
-            "algorithmic_bytes": int(byts), "tb_s": round(byts / (ms * 1e-3) / 1e12, 4),
-            "full_head_bytes": int(full_head), "bound": "hbm (low-rank head + gathered candidate rows)"}
+    return res
 
 
 def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
@@ -572,8 +590,15 @@ def run_tree_prune(step, w, args, flush, stream, costs=(1.0, 10.0, 0.05)):
     n = int(out["n"].item())
     W = (n + 63) // 64
     byts = B * m * (4 * 4 + 8) + B * n * (4 * 5 + 8 + 8 * W) + B * 4
-    return {"ms": round(ms, 5), "costs": list(costs), "n": n, "algorithmic_bytes": int(byts),
-            "bound": "latency (three small launches)"}
+    res = {"ms": round(ms, 5), "costs": list(costs), "n": n, "algorithmic_bytes": int(byts),
+           "bound": "latency (three small launches)"}
+    if not args.no_cpu_baseline and _WORLD == 1:
+        import oracle
+        hh = {k: v.cpu().numpy() for k, v in tree.items()}
+        t0 = time.perf_counter()
+        oracle.tree_prune(hh["tokens"], hh["parents"], hh["depth"], hh["values"], *costs, node_row=hh["node_row"])
+        res["oracle_ms"] = round((time.perf_counter() - t0) * 1e3, 2)
+    return res
 
 
 def run_kv_commit(step, w, args, flush, stream, world):
@@ -734,11 +759,14 @@ def run_reference(args, rank, world):
 # distributed plumbing (replicas only: no data-path collective)
 # ------------------------------------------------------------------------------------
 _PG = None
+_WORLD = 1
 
 
 def init_dist(args):
     global _PG
+    global _WORLD
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    _WORLD = world
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
