@@ -66,14 +66,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // KT == 0: running (max, first index) over the CTA's columns -> part_v / part_i [M, S].
-// KT >= 1: the KT best columns (value descending, ties -> lower index) of every vocabulary tile
-// of vt consecutive 256-column tiles -> cand [M, C] at KT * (vocabulary tile) (-1 where a tile
-// has fewer columns); the CTA's tile range starts on a vocabulary-tile boundary.
+// KT >= 1: a vocabulary tile is vt consecutive 256-column tiles, split into vs parts of pt = vt/vs
+// tiles; for every part, the KT best columns (value descending, ties -> lower index) with their
+// values -> plv / pli [M, NV, vs, KT] (index INT_MAX where a part has fewer columns).  The CTA's
+// tile range starts on a part boundary; gather_logits_kernel merges the parts of a tile.
 template <int KT>
 __global__ void __launch_bounds__(THREADS, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap tma_h, const __grid_constant__ CUtensorMap tma_w,
                    int M, int N, int K, int tpg, float* __restrict__ part_v, int* __restrict__ part_i,
-                   int S, int vt, int32_t* __restrict__ cand, int C, int32_t* status) {
+                   int S, int vt, int pt, int vs, float* __restrict__ plv, int* __restrict__ pli, int32_t* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -227,11 +228,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(acc_empty(ab));
       if (KT > 0) {
         const int t = tile0 + i;
-        if ((t + 1) % vt == 0 || t == NT - 1) {  // a vocabulary tile ends here
+        if ((t + 1) % pt == 0 || t == NT - 1) {  // a part of a vocabulary tile ends here
           if (row < M && !*abort_flag) {
-            const long long o = static_cast<long long>(row) * C + static_cast<long long>(t / vt) * KL;
+            const int NV = (NT + vt - 1) / vt;
+            const long long o = ((static_cast<long long>(row) * NV + t / vt) * vs + (t % vt) / pt) * KL;
 #pragma unroll
-            for (int e = 0; e < KL; ++e) cand[o + e] = li[e] == INT_MAX ? -1 : li[e];
+            for (int e = 0; e < KL; ++e) {
+              plv[o + e] = lv[e];
+              pli[o + e] = li[e];
+            }
           }
 #pragma unroll
           for (int e = 0; e < KL; ++e) {
@@ -312,15 +317,39 @@ __global__ void __launch_bounds__(256) lowrank_proj_kernel(const __nv_bfloat16* 
   if (lane == 0) u[static_cast<long long>(row) * rank + j] = __float2bfloat16_rn(acc);
 }
 
-// One warp per candidate: logits[row][c] = W[cand] . h[row] (fp32), -inf for an empty slot.
+// One warp per candidate slot c = (vocabulary tile, rank e < kt).  The warp first merges the
+// tile's part lists (value descending, ties -> lower id; lane j holds entry j, at most 32) and
+// takes the e-th best as the candidate (-1 when the tile has fewer columns), writes it to cand,
+// then computes logits[row][c] = W[cand] . h[row] (fp32), -inf for an empty slot.
 __global__ void __launch_bounds__(256) gather_logits_kernel(const __nv_bfloat16* __restrict__ hidden,
                                                            const __nv_bfloat16* __restrict__ weight, int V, int d,
-                                                           const int32_t* __restrict__ cand, int C,
+                                                           const float* __restrict__ plv, const int* __restrict__ pli,
+                                                           int kt, int vt, int pt, int vs, int NT,
+                                                           int32_t* __restrict__ cand, int C,
                                                            float* __restrict__ logits, int32_t* status) {
   pdl_wait();
   const int row = blockIdx.x, c = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (c >= C) return;
-  const int id = cand[static_cast<long long>(row) * C + c];
+  const int vtile = c / kt, e = c % kt;
+  const int NV = (NT + vt - 1) / vt;
+  const int parts = (min(vt, NT - vtile * vt) + pt - 1) / pt;  // parts that hold columns
+  const int n = parts * kt;
+  float v = -INFINITY;
+  int vid = INT_MAX;
+  if (lane < n) {
+    const long long o = (static_cast<long long>(row) * NV + vtile) * vs * kt + lane;
+    v = plv[o];
+    vid = pli[o];
+  }
+  int rank = 0;
+  for (int j = 0; j < n; ++j) {
+    const float vj = __shfl_sync(0xffffffffu, v, j);
+    const int ij = __shfl_sync(0xffffffffu, vid, j);
+    rank += ij != INT_MAX && (vj > v || (vj == v && ij < vid));
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < n && vid != INT_MAX && rank == e);
+  const int id = hit ? __shfl_sync(0xffffffffu, vid, __ffs(hit) - 1) : -1;
+  if (lane == 0) cand[static_cast<long long>(row) * C + c] = id;
   float acc = -INFINITY;
   if (id >= 0 && id < V) {
     const uint4* h4 = reinterpret_cast<const uint4*>(hidden + static_cast<long long>(row) * d);
@@ -457,16 +486,29 @@ static bool encode_rows(CUtensorMap* map, const void* base, int rows, int K, int
 
 // Vocabulary tiles per CTA: with MT row tiles, about one wave of CTAs (the MT CTAs of one
 // vocabulary range are adjacent in launch order, so they share the weight tiles in L2).
-static void plan(int M, int N, int num_sms, int* groups, int* tpg, int vt = 1) {
+// With vocabulary tiles of vt GEMM tiles (the efficient head's local top-k), a tile is split into
+// vs parts (a power of two dividing vt, with vs * kt <= 32 part-list entries per tile) when that
+// brings the grid closer to one wave; a CTA takes whole parts.
+static void plan(int M, int N, int num_sms, int* groups, int* tpg, int vt = 1, int kt = 1, int* pt_out = nullptr,
+                 int* vs_out = nullptr) {
   const int MT = (M + BM - 1) / BM;
   const int NT = (N + BN - 1) / BN;
-  const int NV = (NT + vt - 1) / vt;  // vocabulary tiles; a CTA takes whole ones
-  int G = num_sms / MT;
-  if (G < 1) G = 1;
-  if (G > NV) G = NV;
-  const int t = (NV + G - 1) / G * vt;
+  const int NV = (NT + vt - 1) / vt;  // vocabulary tiles
+  int cap = num_sms / MT;
+  if (cap < 1) cap = 1;
+  int vs = 1;
+  while (2 * vs <= vt && vt % (2 * vs) == 0 && 2 * vs * kt <= 32 &&
+         static_cast<long long>(NV) * 2 * vs <= cap)
+    vs *= 2;
+  const int pt = vt / vs;
+  const int NP = (NT + pt - 1) / pt;  // parts; a CTA takes whole ones
+  int G = cap;
+  if (G > NP) G = NP;
+  const int t = (NP + G - 1) / G * pt;
   *tpg = t;
   *groups = (NT + t - 1) / t;
+  if (pt_out) *pt_out = pt;
+  if (vs_out) *vs_out = vs;
 }
 
 }  // namespace lm
@@ -497,7 +539,8 @@ int lm_head_partials_launch(const void* hidden, const void* weight, int M, int N
   if (attr_err != cudaSuccess) return TS_ERR_CUDA;
   const int MT = (M + lm::BM - 1) / lm::BM;
   if (launch_pdl(lm::lm_head_kernel<0>, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, N, K,
-                 tpg, part_v, part_i, G, 1, static_cast<int32_t*>(nullptr), 0, dev_status) != cudaSuccess)
+                 tpg, part_v, part_i, G, 1, 1, 1, static_cast<float*>(nullptr), static_cast<int*>(nullptr),
+                 dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   count_launches(1);
   *S_out = G;
@@ -528,12 +571,16 @@ int efficient_head_candidates(int V, int tile_tokens, int k_tile) {
 size_t efficient_head_workspace_bytes(int M, int V, int rank, int tile_tokens, int k_tile) {
   const size_t C = static_cast<size_t>(efficient_head_candidates(V, tile_tokens, k_tile));
   const size_t u = (static_cast<size_t>(M) * rank * 2 + 255) / 256 * 256;
-  return u + static_cast<size_t>(M) * C * 8 + 256;
+  // part lists: at most tile_tokens / 256 parts per vocabulary tile, k_tile (value, id) each
+  const size_t vt = static_cast<size_t>(tile_tokens / lm::BN);
+  const size_t parts = (static_cast<size_t>(M) * (C / k_tile) * vt * k_tile * 8 + 255) / 256 * 256;
+  return u + static_cast<size_t>(M) * C * 8 + parts + 256;
 }
 
 template <int KT>
 static cudaError_t launch_scores(const CUtensorMap& mh, const CUtensorMap& mw, int M, int V, int rank, int tpg,
-                                 int G, int vt, int32_t* cand, int C, int32_t* status, cudaStream_t stream) {
+                                 int G, int vt, int pt, int vs, float* plv, int* pli, int32_t* status,
+                                 cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -543,7 +590,8 @@ static cudaError_t launch_scores(const CUtensorMap& mh, const CUtensorMap& mw, i
   if (attr_err != cudaSuccess) return attr_err;
   const int MT = (M + lm::BM - 1) / lm::BM;
   return launch_pdl(lm::lm_head_kernel<KT>, dim3(MT, G), dim3(lm::THREADS), lm::SMEM_BYTES, stream, mh, mw, M, V,
-                    rank, tpg, static_cast<float*>(nullptr), static_cast<int*>(nullptr), 0, vt, cand, C, status);
+                    rank, tpg, static_cast<float*>(nullptr), static_cast<int*>(nullptr), 0, vt, pt, vs, plv, pli,
+                    status);
 }
 
 int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a, const void* weight, int M, int V,
@@ -556,32 +604,37 @@ int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a
   const size_t u_bytes = (static_cast<size_t>(M) * rank * 2 + 255) / 256 * 256;
   int32_t* cand = cand_out != nullptr ? cand_out : reinterpret_cast<int32_t*>(ws + u_bytes);
   float* logits = reinterpret_cast<float*>(ws + u_bytes + static_cast<size_t>(M) * C * 4);
+  const int vt = tile_tokens / lm::BN;
+  const size_t nv = static_cast<size_t>(C / k_tile);
+  float* plv = reinterpret_cast<float*>(ws + u_bytes + static_cast<size_t>(M) * C * 8);
+  int* pli = reinterpret_cast<int*>(plv + static_cast<size_t>(M) * nv * vt * k_tile);
   // 1. u = bf16(B h)
   if (launch_pdl(lm::lowrank_proj_kernel, dim3(M, (rank + 7) / 8), dim3(256), 0, stream,
                  static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(lr_b), d, rank, u) !=
       cudaSuccess)
     return TS_ERR_CUDA;
-  // 2. scores = A u with the local top-k_tile of every vocabulary tile
-  const int vt = tile_tokens / lm::BN;
-  int G, tpg;
-  lm::plan(M, V, num_sms, &G, &tpg, vt);
+  // 2. scores = A u with the local top-k_tile of every part of every vocabulary tile
+  int G, tpg, pt, vs;
+  lm::plan(M, V, num_sms, &G, &tpg, vt, k_tile, &pt, &vs);
   CUtensorMap mu, ma;
   if (!lm::encode_rows(&mu, u, M, rank, lm::BM) || !lm::encode_rows(&ma, lr_a, V, rank, lm::BN)) return TS_ERR_CUDA;
   cudaError_t e;
   switch (k_tile) {
-    case 1: e = launch_scores<1>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 2: e = launch_scores<2>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 3: e = launch_scores<3>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 4: e = launch_scores<4>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 5: e = launch_scores<5>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 6: e = launch_scores<6>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    case 7: e = launch_scores<7>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
-    default: e = launch_scores<8>(mu, ma, M, V, rank, tpg, G, vt, cand, C, dev_status, stream); break;
+    case 1: e = launch_scores<1>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 2: e = launch_scores<2>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 3: e = launch_scores<3>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 4: e = launch_scores<4>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 5: e = launch_scores<5>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 6: e = launch_scores<6>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    case 7: e = launch_scores<7>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
+    default: e = launch_scores<8>(mu, ma, M, V, rank, tpg, G, vt, pt, vs, plv, pli, dev_status, stream); break;
   }
   if (e != cudaSuccess) return TS_ERR_CUDA;
-  // 3. exact logits of the candidates
+  // 3. the candidates (merged part lists) and their exact logits
+  const int NT = (V + lm::BN - 1) / lm::BN;
   if (launch_pdl(lm::gather_logits_kernel, dim3(M, (C + 7) / 8), dim3(256), 0, stream,
-                 static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(weight), V, d, cand, C,
+                 static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(weight), V, d,
+                 static_cast<const float*>(plv), static_cast<const int*>(pli), k_tile, vt, pt, vs, NT, cand, C,
                  logits, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   // 4. the k best candidates and their log-probabilities over the candidate set
