@@ -65,6 +65,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Sorted (value descending) list of KL entries in registers: insert (cv, ci) without branches.
+// The new list is computed from the old one: entry e becomes cv where cv is better than the old
+// entry e but not than entry e-1, the old entry e-1 where cv is better than both, else stays.
+// `full` compares (value, then lower index); without it a strict value compare is enough,
+// because a list fed columns in increasing order keeps the earlier of equal values.
+template <int KL, bool full>
+__device__ __forceinline__ void list_insert(float (&v)[KL], int (&id)[KL], float cv, int ci) {
+#pragma unroll
+  for (int e = KL - 1; e >= 0; --e) {
+    const bool gt = full ? (cv > v[e] || (cv == v[e] && ci < id[e])) : cv > v[e];
+    bool gtp = false;
+    if (e > 0) gtp = full ? (cv > v[e - 1] || (cv == v[e - 1] && ci < id[e - 1])) : cv > v[e - 1];
+    const float nv = gtp ? v[e > 0 ? e - 1 : 0] : cv;
+    const int ni = gtp ? id[e > 0 ? e - 1 : 0] : ci;
+    v[e] = gt ? nv : v[e];
+    id[e] = gt ? ni : id[e];
+  }
+}
+
 // KT == 0: running (max, first index) over the CTA's columns -> part_v / part_i [M, S].
 // KT >= 1: a vocabulary tile is vt consecutive 256-column tiles, split into vs parts of pt = vt/vs
 // tiles; for every part, the KT best columns (value descending, ties -> lower index) with their
@@ -189,6 +208,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       lv[e] = -INFINITY;
       li[e] = INT_MAX;
     }
+    // KT >= 1: a second list takes the odd columns (two independent dependency chains, no
+    // branches); the two are merged when a part ends
+    float ov[KL];
+    int oi[KL];
+#pragma unroll
+    for (int e = 0; e < KL; ++e) {
+      ov[e] = -INFINITY;
+      oi[e] = INT_MAX;
+    }
     const int row = mt * BM + r;
     for (int i = 0; i < ntile; ++i) {
       const int ab = i & 1;
@@ -200,25 +228,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t u[32];
         tmem_ld32(tmem + lane_off + ab * BN + 32u * c, u);
         const int nb = n0 + 32 * c;
+        if constexpr (KT > 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float cv = __uint_as_float(u[j]);
-          if (nb + j < N && cv > lv[KL - 1]) {
-            // columns arrive in increasing order: a strict > keeps the earlier of equal values
-            // insert before the first smaller entry; everything after it shifts down by one
-            int ci = nb + j;
-            bool shift = false;
+          for (int j = 0; j < 32; j += 2) {
+            list_insert<KL, false>(lv, li, nb + j < N ? __uint_as_float(u[j]) : -INFINITY, nb + j);
+            list_insert<KL, false>(ov, oi, nb + j + 1 < N ? __uint_as_float(u[j + 1]) : -INFINITY, nb + j + 1);
+          }
+        } else {
 #pragma unroll
-            for (int e = 0; e < KL; ++e) {
-              if (shift || cv > lv[e]) {
-                const float tv = lv[e];
-                const int ti = li[e];
-                lv[e] = cv;
-                li[e] = ci;
-                cv = tv;
-                ci = ti;
-                shift = true;
-              }
+          for (int j = 0; j < 32; ++j) {  // the running maximum, first index on ties
+            const float cv = __uint_as_float(u[j]);
+            if (nb + j < N && cv > lv[0]) {
+              lv[0] = cv;
+              li[0] = nb + j;
             }
           }
         }
@@ -229,6 +251,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (KT > 0) {
         const int t = tile0 + i;
         if ((t + 1) % pt == 0 || t == NT - 1) {  // a part of a vocabulary tile ends here
+#pragma unroll
+          for (int e = 0; e < KL; ++e) {  // merge the odd-column list in
+            list_insert<KL, true>(lv, li, ov[e], oi[e]);
+            ov[e] = -INFINITY;
+            oi[e] = INT_MAX;
+          }
           if (row < M && !*abort_flag) {
             const int NV = (NT + vt - 1) / vt;
             const long long o = ((static_cast<long long>(row) * NV + t / vt) * vs + (t % vt) / pt) * KL;
