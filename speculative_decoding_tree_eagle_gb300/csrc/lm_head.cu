@@ -402,8 +402,70 @@ __global__ void __launch_bounds__(256) gather_logits_kernel(const __nv_bfloat16*
   if (lane == 0) logits[static_cast<long long>(row) * C + c] = acc;
 }
 
-// One CTA per row: the k best candidates (logit descending, ties -> lower id) and their
-// log-probabilities over the candidate set (logit - logsumexp of the candidates' logits).
+// One warp per row, for candidate sets of at most kHeadWarpMaxC: the same k best candidates
+// and log-probabilities as head_topk_kernel below.  Every lane keeps the best of its own share
+// (a stride-32 slice in shared memory); a pick is a 5-step shuffle reduction of the 32 lane
+// bests, after which only the lane that held the pick rescans its share.  No block barrier.
+constexpr int kHeadRows = 4;
+constexpr int kHeadWarpMaxC = 1024;
+__global__ void __launch_bounds__(kHeadRows * 32) head_topk_warp_kernel(const float* __restrict__ logits,
+                                                                       const int32_t* __restrict__ cand, int M,
+                                                                       int C, int k, int32_t* __restrict__ top_tok,
+                                                                       float* __restrict__ top_logp) {
+  extern __shared__ unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* sl = reinterpret_cast<float*>(smem_raw) + static_cast<size_t>(warp) * 2 * C;
+  int* si = reinterpret_cast<int*>(sl + C);
+  pdl_wait();
+  const int row = blockIdx.x * kHeadRows + warp;
+  if (row >= M) return;
+  const float* lr = logits + static_cast<long long>(row) * C;
+  const int32_t* cr = cand + static_cast<long long>(row) * C;
+  float mx = -INFINITY, bv = -INFINITY;
+  int bi = INT_MAX, bc = -1;
+  for (int c = lane; c < C; c += 32) {
+    const int id = cr[c];
+    const float l = id >= 0 ? lr[c] : -INFINITY;
+    const int ii = id >= 0 ? id : INT_MAX;
+    sl[c] = l;
+    si[c] = ii;
+    mx = fmaxf(mx, l);
+    if (better(l, ii, bv, bi)) bv = l, bi = ii, bc = c;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+  for (int c = lane; c < C; c += 32)
+    if (sl[c] != -INFINITY) sum += expf(sl[c] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float lse = mx + logf(sum);
+  for (int j = 0; j < k; ++j) {
+    float v = bv;
+    int i = bi;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+      if (better(ov, oi, v, i)) v = ov, i = oi;
+    }
+    if (lane == 0) {
+      top_tok[static_cast<long long>(row) * k + j] = i == INT_MAX ? -1 : i;
+      top_logp[static_cast<long long>(row) * k + j] = i == INT_MAX ? -INFINITY : v - lse;
+    }
+    if (i != INT_MAX && bi == i) {  // this lane held the pick: take it out, find its next best
+      sl[bc] = -INFINITY;
+      si[bc] = INT_MAX;
+      bv = -INFINITY, bi = INT_MAX, bc = -1;
+      for (int c = lane; c < C; c += 32)
+        if (better(sl[c], si[c], bv, bi)) bv = sl[c], bi = si[c], bc = c;
+    }
+  }
+}
+
+// One CTA per row (larger candidate sets): the k best candidates (logit descending, ties ->
+// lower id) and their log-probabilities over the candidate set (logit - logsumexp of the
+// candidates' logits).
 constexpr int kHeadThreads = 256;
 __device__ __forceinline__ void block_best_pair(float& v, int& i, float* s_v, int* s_i) {
 #pragma unroll
@@ -666,6 +728,14 @@ int efficient_head_launch(const void* hidden, const void* lr_b, const void* lr_a
                  logits, dev_status) != cudaSuccess)
     return TS_ERR_CUDA;
   // 4. the k best candidates and their log-probabilities over the candidate set
+  if (C <= lm::kHeadWarpMaxC) {
+    if (launch_pdl(lm::head_topk_warp_kernel, dim3((M + lm::kHeadRows - 1) / lm::kHeadRows), dim3(lm::kHeadRows * 32),
+                   static_cast<size_t>(lm::kHeadRows) * C * 8, stream, logits, cand, M, C, k, top_tok,
+                   top_logp) != cudaSuccess)
+      return TS_ERR_CUDA;
+    count_launches(4);
+    return TS_OK;
+  }
   const size_t smem = static_cast<size_t>(C) * 8;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(lm::head_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=

@@ -10,13 +10,15 @@
 // head-in-group, so every K/V byte fetched from HBM serves m*g query rows on the tensor
 // cores.  A row group is one (NM = 1) or two (NM = 2) 128-row M tiles.  One CTA per SM.
 //
-// Warp roles (128*(1+NM) + 128 + 32 threads):
-//   warps 0,2,3,last  warp 0 stages the chunk's physical block ids in shared memory; then
-//               one thread in each of four warps issues TMA loads (K: warps 0 and 3, V: warp
-//               2 and the last warp, half of each tile's boxes each): per 64-key tile one box
-//               of min(block_size,64) rows x 64 bf16 (128-byte swizzle) per page and
-//               head-dim half; positions past the sequence load an out-of-range block (zero
-//               fill).  STAGES-deep ring; each full barrier expects both producers.
+// Warp roles (4 + 4*NM warps, then the extra producer warps; 288 threads for NM = 1, 384 for 2):
+//   warps 0,2,3 and the warps after the softmax warps
+//               warp 0 stages the chunk's physical block ids in shared memory; then one
+//               thread per producer warp issues TMA loads (K: warps 0 and 3; V: warp 2 and,
+//               for one-tile groups, the last warp; each an even share of every tile's
+//               boxes): per 64-key tile one box of min(block_size,64) rows x 64 bf16
+//               (128-byte swizzle) per page and head-dim half; positions past the sequence
+//               load an out-of-range block (zero fill).  STAGES-deep ring; each full barrier
+//               expects every producer of its operand.
 //   warp 1      TMEM allocator + the single thread that issues tcgen05.mma:
 //                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
 //                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
@@ -72,11 +74,17 @@ template <int NM>
 struct Cfg {
   static constexpr int SB = NM == 1 ? 2 : 1;  // S / P buffers per M tile
   static constexpr int STAGES = NM == 1 ? 5 : 4;
-  // one-tile groups are bandwidth-bound and get a fourth TMA-issuing warp; two-tile groups
-  // stay at 12 warps to keep 170 registers per thread
-  static constexpr int THREADS = 128 + 128 * NM + (NM == 1 ? 32 : 0);
-  static constexpr int EXTRA_WARP = 4 + 4 * NM;  // == THREADS / 32 when there is no extra warp
+  // A TMA instruction holds its issuing thread for a while (~0.19 us for a page-sized box),
+  // so the boxes of a tile are spread over K_PRODUCERS + V_PRODUCERS warps.  Two-tile groups
+  // are bound by their MMAs (a tile takes ~1.7 us, ~142 cycles per tcgen05.mma, against
+  // ~0.8 us of box issue per producer warp) and keep a single V warp; more producer warps
+  // (up to four of each) measured no faster in either group.  Warps 0 and 3 issue K, warp 2
+  // V, and the warps after the softmax warps (from EXTRA_WARP on) the remaining V parts,
+  // then K parts.
+  static constexpr int K_PRODUCERS = 2;
   static constexpr int V_PRODUCERS = NM == 1 ? 2 : 1;
+  static constexpr int EXTRA_WARP = 4 + 4 * NM;
+  static constexpr int THREADS = 32 * (EXTRA_WARP + (K_PRODUCERS - 2) + (V_PRODUCERS - 1));
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 128 * NM;
   static constexpr uint32_t COL_P = COL_S + 64 * NM * SB;
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
-      mbar_init(full_k(s), 2);  // each producer warp registers its own bytes
+      mbar_init(full_k(s), C::K_PRODUCERS);  // each producer warp registers its own bytes
       mbar_init(full_v(s), C::V_PRODUCERS);
       mbar_init(empty_k(s), 1);
       mbar_init(empty_v(s), 1);
@@ -264,18 +272,18 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
   bool ok = true;
 
-  if (warp == 0 || warp == 2 || warp == 3 || warp == C::EXTRA_WARP) {
+  if (warp == 0 || warp == 2 || warp == 3 || warp >= C::EXTRA_WARP) {
     // ------------------------------ TMA producers ------------------------------
-    // A TMA instruction holds its issuing thread for a while, so page-sized boxes are issued
-    // from several warps: K tiles by warps 0 and 3 (half of each tile's boxes each), V tiles
-    // by warp 2, and for one-tile groups also by the extra warp (again half each).
+    // Part `part` of `nparts` issues boxes [part*nbox/nparts, (part+1)*nbox/nparts) of every
+    // tile (a part may hold none: it still registers its zero bytes once per tile).
     if (lane == 0) {
-      const int kv = (warp == 0 || warp == 3) ? 0 : 1;
-      const int part = (warp == 0 || warp == 2) ? 0 : 1;
-      const int nparts = kv == 0 ? 2 : C::V_PRODUCERS;
+      const int e = warp - C::EXTRA_WARP;  // index among the warps after the softmax warps
+      const int kv = (warp == 0 || warp == 3 || (e >= 0 && e >= C::V_PRODUCERS - 1)) ? 0 : 1;
+      const int part = warp == 0 ? 0 : warp == 3 ? 1 : warp == 2 ? 0 : kv == 1 ? e + 1 : 2 + e - (C::V_PRODUCERS - 1);
+      const int nparts = kv == 0 ? C::K_PRODUCERS : C::V_PRODUCERS;
       const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
       const int nbox = 2 * bpt;                    // boxes per tile: pages x head-dim halves
-      const int b_begin = part * (nbox / 2), b_end = (part == 0 && nparts == 2) ? nbox / 2 : nbox;
+      const int b_begin = part * nbox / nparts, b_end = (part + 1) * nbox / nparts;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % ST;
@@ -395,13 +403,10 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         tc_fence_after();
         float s[BN];
         {
-          uint32_t u[32];
-          tmem_ld32(tS, u);
+          uint32_t u[BN];
+          tmem_ld64(tS, u);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(u[c]);
-          tmem_ld32(tS + 32, u);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(u[c]);
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
         }
         const int key0 = (t0 + t) * BN;
         float mx = -INFINITY;
@@ -418,13 +423,15 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
           if (ntree < 64) tb &= ntree > 0 ? (1ull << ntree) - 1ull : 0ull;
           const uint64_t vis = pre > 0 ? (((1ull << pre) - 1ull) | (tb << pre)) : tb;
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            s[c] = ((vis >> c) & 1ull) ? s[c] : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-          }
-        } else {
+          for (int c = 0; c < BN; ++c) s[c] = ((vis >> c) & 1ull) ? s[c] : -INFINITY;
+        }
+        {  // eight independent running maxima, then a tree
+          float m8[8];
 #pragma unroll
-          for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < 8; ++c) m8[c] = s[c];
+#pragma unroll
+          for (int c = 8; c < BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         if (!valid) mx = -INFINITY;
         const float mt = mx * sl2;
@@ -440,15 +447,15 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[32];
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const float p0 = valid ? ex2_approx(fmaf(s[2 * c], sl2, -mu)) : 0.f;
           const float p1 = valid ? ex2_approx(fmaf(s[2 * c + 1], sl2, -mu)) : 0.f;
-          rs += p0 + p1;
+          rs4[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l_sum += rs;
+        l_sum += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         tmem_st32(tP, pk);
         if (__any_sync(0xffffffffu, resc)) {
           // O must hold P V of tile t-1 before it is rescaled

@@ -30,7 +30,10 @@ CASES = [dict(M=7, V=3000, d=128, rank=32, tile_tokens=256, k_tile=3, k=10),
          dict(M=130, V=10000, d=64, rank=16, tile_tokens=512, k_tile=8, k=16),
          dict(M=1, V=256, d=8, rank=8, tile_tokens=256, k_tile=1, k=1),
          dict(M=33, V=5000, d=96, rank=24, tile_tokens=1024, k_tile=4, k=8),
-         dict(M=80, V=128256, d=4096, rank=256, tile_tokens=1024, k_tile=2, k=10, b_density=1 / 64)]
+         dict(M=80, V=128256, d=4096, rank=256, tile_tokens=1024, k_tile=2, k=10, b_density=1 / 64),
+         # 1024 candidates: the largest set the warp-per-row top-k takes; 1256: one CTA per row
+         dict(M=9, V=32768, d=64, rank=16, tile_tokens=256, k_tile=8, k=16),
+         dict(M=6, V=40000, d=64, rank=16, tile_tokens=256, k_tile=8, k=12)]
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"M{c['M']}_V{c['V']}_d{c['d']}_r{c['rank']}_T{c['tile_tokens']}_kt{c['k_tile']}")
