@@ -266,7 +266,9 @@ int ts_tree_accept_hidden(const void* hidden, const void* weight, const int32_t*
  * candidates [M, C], C = ts_efficient_head_candidates(V, tile_tokens, k_tile) (-1 in empty
  * slots);  logits[c] = weight[c] @ h (weight [V, d], fp32);  top_tok [M, k] = the k best
  * candidates (logit descending, ties -> lower id), top_logp [M, k] = logit - logsumexp over
- * the candidates' logits.  Rows of top_tok / top_logp are what ts_tree_build_from_topk reads.
+ * the candidates' logits; where short tiles leave a row fewer than k candidates, its last
+ * entries are top_tok -1, top_logp -inf.  Rows of top_tok / top_logp are what
+ * ts_tree_build_from_topk reads.
  * All bf16 tensors row-major, device, 16-byte aligned; d % 8 == 0, rank % 8 == 0,
  * tile_tokens % 256 == 0, 1 <= k_tile <= 8, 1 <= k <= min(16, C).  candidates may be NULL.
  * Four launches on `stream`; workspace of ts_efficient_head_workspace(...) bytes.

@@ -61,12 +61,14 @@ def candidates(hidden, lr_b, lr_a, tile_tokens: int, k_tile: int) -> np.ndarray:
 
 
 def efficient_head(hidden, lr_b, lr_a, weight, tile_tokens: int, k_tile: int, k: int):
-    """Returns (top_tok int64 [M, k], top_logp fp64 [M, k], candidates int64 [M, C])."""
+    """Returns (top_tok int64 [M, k], top_logp fp64 [M, k], candidates int64 [M, C]).  When short
+    tiles leave a row fewer than k candidates, its remaining entries are token -1 with
+    log-probability -inf (a reading: the pages do not meet the case)."""
     h, W = _f64(hidden), _f64(weight)
     cand = candidates(hidden, lr_b, lr_a, tile_tokens, k_tile)
     M = h.shape[0]
-    tok = np.zeros((M, k), dtype=np.int64)
-    lp = np.zeros((M, k))
+    tok = np.full((M, k), -1, dtype=np.int64)
+    lp = np.full((M, k), -np.inf)
     for r in range(M):
         ids = [int(i) for i in cand[r] if i >= 0]
         logits = {i: float(W[i] @ h[r]) for i in ids}

@@ -33,7 +33,9 @@ CASES = [dict(M=7, V=3000, d=128, rank=32, tile_tokens=256, k_tile=3, k=10),
          dict(M=80, V=128256, d=4096, rank=256, tile_tokens=1024, k_tile=2, k=10, b_density=1 / 64),
          # 1024 candidates: the largest set the warp-per-row top-k takes; 1256: one CTA per row
          dict(M=9, V=32768, d=64, rank=16, tile_tokens=256, k_tile=8, k=16),
-         dict(M=6, V=40000, d=64, rank=16, tile_tokens=256, k_tile=8, k=12)]
+         dict(M=6, V=40000, d=64, rank=16, tile_tokens=256, k_tile=8, k=12),
+         # a one-id last tile: 9 candidates for k = 16, the last 7 entries are -1 / -inf
+         dict(M=3, V=257, d=64, rank=16, tile_tokens=256, k_tile=8, k=16)]
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"M{c['M']}_V{c['V']}_d{c['d']}_r{c['rank']}_T{c['tile_tokens']}_kt{c['k_tile']}")

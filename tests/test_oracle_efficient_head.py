@@ -56,6 +56,20 @@ def test_short_tile_and_ties():
     assert list(tok[0]) == [4, 1, 0]          # logits 5, 2, 1; id 2 (logit 2) is not a candidate
 
 
+def test_fewer_candidates_than_k_pad_with_minus_one_and_minus_inf():
+    """Three candidates for k = 4: the three by logit (5, 2, 1) with log-probabilities from the
+    closed-form logsumexp over exactly those three logits, then one padding entry."""
+    h = torch.tensor([[1.0, 0.0]]).to(torch.bfloat16)
+    B = torch.tensor([[1.0, 0.0], [0.0, 1.0]]).to(torch.bfloat16)
+    A = torch.tensor([[1.0, 0.0]] * 5).to(torch.bfloat16)
+    W = torch.tensor([[1.0, 0.0], [2.0, 0.0], [2.0, 0.0], [0.0, 0.0], [5.0, 0.0]]).to(torch.bfloat16)
+    tok, lp, _ = oracle.efficient_head(h, B, A, W, tile_tokens=4, k_tile=2, k=4)
+    assert list(tok[0]) == [4, 1, 0, -1]
+    lse = math.log(math.exp(5) + math.exp(2) + math.exp(1))
+    np.testing.assert_allclose(lp[0, :3], [5 - lse, 2 - lse, 1 - lse], rtol=0, atol=1e-12)
+    assert lp[0, 3] == -math.inf
+
+
 def test_one_tile_is_global_topk_on_the_low_rank_scores():
     h, B, A, W = _case(11, V=30)
     cand = oracle.efficient_head(h, B, A, W, tile_tokens=64, k_tile=6, k=2)[2]
