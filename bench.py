@@ -102,6 +102,22 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def attention_roofline(attn_bytes, attn_flops, attn_ms, hbm, tensor, traffic):
+    """The attention call against its binding roof: the HBM copy bandwidth (algorithmic bytes /
+    time), or the tensor pipe (FLOPs / time) where its FLOPs take longer at the bf16 peak than
+    its bytes at the HBM peak (FLOPs per K/V byte, about m*g, past the ridge).  `hbm` and
+    `tensor` are (peak, kind) pairs in GB/s and TFLOP/s."""
+    (hbm_gbs, hbm_kind), (tf, tf_kind) = hbm, tensor
+    kernel = "tree_attention (tcgen05 kernel + split-K combine)"
+    if attn_flops / (tf * 1e12) > attn_bytes / (hbm_gbs * 1e9):
+        achieved = attn_flops / (attn_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": kernel, "achieved": round(achieved, 1), "peak": tf,
+                "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": round(achieved / tf, 4), "traffic": traffic}
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm_gbs, "peak_kind": hbm_kind,
+            "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4), "traffic": traffic}
+
+
 def kernel_source_hash():
     """Hash of the sources the attention kernels are built from (the roofline kernel)."""
     h = hashlib.sha256()
@@ -359,21 +375,9 @@ def run_ours(args, rank, world, dev):
     peak, peak_kind = hbm_peak()
     mean = lambda x: sum(x) / len(x)
     attn_ms = mean(t_attn)
-    achieved_gbs = ab["tree_attention"] / (attn_ms * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
-    # the attention call's binding roof: HBM for its K/V stream, or the tensor pipe where its
-    # FLOPs per K/V byte (about m*g) exceed the ridge of the two measured peaks
-    attn_flops = attention_flops(w, inp["prefix_len"].tolist())
-    tf_peak, tf_kind = tensor_peak()
-    if attn_flops / (tf_peak * 1e12) > ab["tree_attention"] / (peak * 1e9):
-        achieved_tf = attn_flops / (attn_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "tree_attention (tcgen05 kernel + split-K combine)",
-                    "achieved": round(achieved_tf, 1), "peak": tf_peak, "peak_kind": tf_kind, "unit": "TFLOP/s",
-                    "frac": round(achieved_tf / tf_peak, 4), "traffic": traffic}
-    else:
-        roofline = {"bound": "hbm", "kernel": "tree_attention (tcgen05 kernel + split-K combine)",
-                    "achieved": round(achieved_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": round(achieved_gbs / peak, 4), "traffic": traffic}
+    roofline = attention_roofline(ab["tree_attention"], attention_flops(w, inp["prefix_len"].tolist()), attn_ms,
+                                  (peak, peak_kind), tensor_peak(), traffic)
     res = {
         "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5),
