@@ -328,9 +328,7 @@ __global__ void __launch_bounds__(256) lowrank_proj_kernel(const __nv_bfloat16* 
   if (j >= rank) return;
   const uint4* h4 = reinterpret_cast<const uint4*>(hidden + static_cast<long long>(row) * d);
   const uint4* b4 = reinterpret_cast<const uint4*>(lr_b + static_cast<long long>(j) * d);
-  float acc = 0.f;
-  for (int c = lane; c < d / 8; c += 32) {
-    const uint4 x = __ldg(h4 + c), y = __ldg(b4 + c);
+  auto dot8 = [](const uint4& x, const uint4& y, float acc) {
     acc = fmaf(bf16_lo(x.x), bf16_lo(y.x), acc);
     acc = fmaf(bf16_hi(x.x), bf16_hi(y.x), acc);
     acc = fmaf(bf16_lo(x.y), bf16_lo(y.y), acc);
@@ -338,8 +336,27 @@ __global__ void __launch_bounds__(256) lowrank_proj_kernel(const __nv_bfloat16* 
     acc = fmaf(bf16_lo(x.z), bf16_lo(y.z), acc);
     acc = fmaf(bf16_hi(x.z), bf16_hi(y.z), acc);
     acc = fmaf(bf16_lo(x.w), bf16_lo(y.w), acc);
-    acc = fmaf(bf16_hi(x.w), bf16_hi(y.w), acc);
+    return fmaf(bf16_hi(x.w), bf16_hi(y.w), acc);
+  };
+  // eight 16-byte pairs in flight per lane before any is used (a row of 4096 is two batches)
+  const int n8 = d / 8;
+  float acc0 = 0.f, acc1 = 0.f;
+  int c = lane;
+  for (; c + 7 * 32 < n8; c += 8 * 32) {
+    uint4 x[8], y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[e] = __ldg(h4 + c + 32 * e);
+      y[e] = __ldg(b4 + c + 32 * e);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      acc0 = dot8(x[e], y[e], acc0);
+      acc1 = dot8(x[e + 1], y[e + 1], acc1);
+    }
   }
+  for (; c < n8; c += 32) acc0 = dot8(__ldg(h4 + c), __ldg(b4 + c), acc0);
+  float acc = acc0 + acc1;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) u[static_cast<long long>(row) * rank + j] = __float2bfloat16_rn(acc);
