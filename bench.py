@@ -825,11 +825,14 @@ def allreduce_max(x, world, dev):
 
 def main():
     args = parse()
-    rank, world, local = init_dist(args)
     if args.impl == "reference":
+        # the oracle arm uses no GPU and no collective: rank 0 alone runs it, the other
+        # ranks leave at once (no process group is formed)
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
+    rank, world, local = init_dist(args)
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     res, w, inp = run_ours(args, rank, world, dev)
