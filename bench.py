@@ -5,22 +5,33 @@ Llama-shaped workload (inputs resident in HBM).  Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+The default workload is the long-context sweep: batch 4, 32 query / 8 KV heads, head dim 128,
+a 32768-token paged bf16 prefix per sequence, and four draft trees (an 8-node chain and
+dynamic trees of 32, 64 and 128 nodes) over a 128256-token vocabulary.  One step of it is
+one verify step of each of the four trees; its value is the sweep's algorithmic bytes over
+the sum of the four step times.  The line's ``per_config`` object then holds every workload
+measured on its own: the four trees of the sweep and the Llama-2-7B, Llama-3-8B and
+Llama-2-70B shaped workloads (``--no-per-config`` skips the three model-shaped ones).
+
 Metric: effective HBM TB/s of the step = algorithmic bytes (each input byte read once, each
 output byte written once) / step time; also tree nodes verified per second.  The L2 cache
-(129 MB) is flushed by writing a 512 MB buffer before every timed step, outside the timed
-events.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+(129 MB) is flushed by writing a 512 MB buffer before every timed graph replay, outside the
+timed events.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
 workload (the slow plain reference this project is checked against).
 """
 from __future__ import annotations
 
 import os
 
-# numpy's BLAS threads for the CPU oracle leg: every host core, set before numpy loads
+# numpy's BLAS threads for the CPU oracle leg: every host core unless the caller set a
+# count (the single-thread oracle timing runs in a child process with a count of 1)
 _CORES = os.cpu_count() or 1
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, str(_CORES))
+_ORACLE_THREADS = int(os.environ["OPENBLAS_NUM_THREADS"])
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -37,27 +48,73 @@ import torch
 
 import workloads
 
-DEFAULT_WORKLOAD = "llama2_7b"
+# the long-context configuration: one batch shape, four tree sizes
+SWEEPS = {"long_context_sweep": ("long_context_m8", "long_context_m32", "long_context_m64", "long_context_m128")}
+DEFAULT_WORKLOAD = "long_context_sweep"
+# measured on their own beside the default workload (the sweep's trees are measured in it)
+OTHER_CONFIGS = ("llama2_7b", "llama3_8b_gqa", "llama2_70b_gqa")
 METRIC = "tree-verify effective HBM TB/s (% of GB300 peak) and tree nodes verified/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS) + sorted(SWEEPS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefix", type=int, default=None,
                     help="override the workload's prefix length (a smaller case for detailed profiling; "
                          "the JSON line then names the modified workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only --workload (no model-shaped configurations beside it)")
+    ap.add_argument("--no-next-rows", action="store_true", help="skip the rows after the hot path")
     ap.add_argument("--no-graph", action="store_true", help="launch through the API each step instead of "
                     "replaying CUDA graphs of the three operations")
-    return ap.parse_args()
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-budget", type=float, default=None, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def workload_list(name, prefix=None):
+    """The workloads one step of ``name`` runs: one, or the four trees of a sweep."""
+    names = SWEEPS.get(name, (name,))
+    out = []
+    for n in names:
+        w = workloads.WORKLOADS[n]
+        if prefix is not None:
+            w = dataclasses.replace(w, name=f"{w.name}_prefix{prefix}", prefix=(prefix, prefix))
+        out.append(w)
+    return out
+
+
+def workload_name(name, prefix=None):
+    return name if prefix is None else f"{name}_prefix{prefix}"
+
+
+def launch_desc(args):
+    if args.no_graph:
+        return "API calls"
+    return ("one CUDA graph per verify step, the three operations' kernels chained by programmatic "
+            "dependent launch; per-operation times are marginal: t(build), t(build+attention) - "
+            "t(build), t(step) - t(build+attention), each a graph replayed after an L2 flush")
+
+
+def config_of(name, args, world):
+    """The ``config`` object of the JSON line (the same for both arms)."""
+    ws = workload_list(name, args.prefix)
+    w0 = ws[0]
+    one = len(ws) == 1
+    pick = (lambda f: f(w0)) if one else (lambda f: [f(w) for w in ws])
+    return {"workload": workload_name(name, args.prefix), "batch": w0.B, "q_heads": w0.Hq, "kv_heads": w0.Hkv,
+            "head_dim": w0.d, "prefix": list(w0.prefix), "tree_nodes": pick(lambda w: w.m),
+            "top_k": pick(lambda w: w.k), "depth": pick(lambda w: w.depth), "vocab": w0.V,
+            "block_size": workloads.BLOCK_SIZE, "l2": "flushed (512 MB write) before every timed graph replay",
+            "launch": launch_desc(args), "parallelism": f"replicas{world}"}
 
 
 # ------------------------------------------------------------------------------------
@@ -116,6 +173,11 @@ def attention_roofline(attn_bytes, attn_flops, attn_ms, hbm, tensor, traffic):
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": hbm_gbs, "peak_kind": hbm_kind,
             "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4), "traffic": traffic}
+
+
+def roof_time_s(attn_bytes, attn_flops, hbm_gbs, tf):
+    """Time of the attention call at its binding roof."""
+    return max(attn_bytes / (hbm_gbs * 1e9), attn_flops / (tf * 1e12))
 
 
 def kernel_source_hash():
@@ -238,12 +300,150 @@ class Step:
         self.accept()
 
 
-def get_workload(args):
-    w = workloads.WORKLOADS[args.workload]
-    if args.prefix is not None:
-        import dataclasses
-        w = dataclasses.replace(w, name=f"{w.name}_prefix{args.prefix}", prefix=(args.prefix, args.prefix))
-    return w
+class Case:
+    """One workload resident on the device with the CUDA graphs that time it.
+
+    ``step`` replays the whole verify step; ``build`` and ``build_attn`` the prefixes of it
+    that give the marginal per-operation times (they sum to the step); ``attn`` the attention
+    call alone (its isolated time, launch latency of a graph included)."""
+
+    def __init__(self, w, args, dev, flush):
+        import speculative_decoding_tree_eagle_gb300 as ts
+        self.ts, self.w = ts, w
+        self.inp = workloads.generate(w)
+        self.step = Step(w, self.inp, dev)
+        step = self.step
+        if w.plant_frac > 0:
+            # the planting recipe needs the draft tree: take it from this library's own tree_build
+            step.build()
+            torch.cuda.synchronize()
+            self.inp["logits"] = workloads.plant_paths(w, self.inp["logits"], step.tree["tokens"].cpu(),
+                                                       step.tree["parents"].cpu())
+            step.d["logits"].copy_(self.inp["logits"])
+        for _ in range(args.warmup):
+            flush.zero_()
+            step.run()
+        torch.cuda.synchronize()
+        ts.check_status(step.status)
+        self.graphs = None
+        self.per_step_launches = None
+        if not args.no_graph:
+            n0 = ts.launch_count()
+            g_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_step):
+                step.run()
+            self.per_step_launches = ts.launch_count() - n0
+            g_b, g_ba, g_a = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_b):
+                step.build()
+            with torch.cuda.graph(g_ba):
+                step.build()
+                step.attention()
+            with torch.cuda.graph(g_a):
+                step.attention()
+            self.graphs = dict(step=g_step, build=g_b, build_attn=g_ba, attn=g_a)
+            for _ in range(2):
+                for g in self.graphs.values():
+                    g.replay()
+            torch.cuda.synchronize()
+        self.ab = algo_bytes(w, self.inp["prefix_len"].tolist())
+        self.flops = attention_flops(w, self.inp["prefix_len"].tolist())
+        self.t = None
+
+    def _run(self, what):
+        if self.graphs is not None:
+            self.graphs[what].replay()
+            return
+        s = self.step
+        if what in ("step", "build", "build_attn"):
+            s.build()
+        if what in ("step", "build_attn", "attn"):
+            s.attention()
+        if what == "step":
+            s.accept()
+
+    def time_steps(self, K, flush, stream):
+        """K timed replays of each graph (step first), L2 flushed before every replay, one
+        event pair around each replay on the launching stream."""
+        kinds = ("step", "build", "build_attn", "attn")
+        evs = {k: [] for k in kinds}
+        n_api = 0
+        for _ in range(K):
+            for k in kinds:
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                n0 = self.ts.launch_count()
+                a.record(stream)
+                self._run(k)
+                b.record(stream)
+                if k == "step":
+                    n_api += self.ts.launch_count() - n0
+                evs[k].append((a, b))
+        torch.cuda.synchronize()
+        self.t = {k: [a.elapsed_time(b) for a, b in v] for k, v in evs.items()}
+        # kernels launched by the K timed steps (a graph replay does not pass through the API's
+        # launch counter, so it counts the captured step's launches once per replay)
+        self.step_launches = self.per_step_launches * K if self.per_step_launches is not None else n_api
+        self.ts.check_status(self.step.status)
+        return self.t
+
+    def summary(self, hbm, tensor, traffic):
+        t = self.t
+        mean = lambda x: sum(x) / len(x)
+        w, ab = self.w, self.ab
+        ms = mean(t["step"])
+        t_b = mean(t["build"])
+        t_ba = mean(t["build_attn"])
+        attn = t_ba - t_b
+        acc = ms - t_ba
+        peak = hbm[0]
+        roof = attention_roofline(ab["tree_attention"], self.flops, attn, hbm, tensor, traffic)
+        t_roof = roof_time_s(ab["tree_attention"], self.flops, hbm[0], tensor[0])
+        aa_bytes = ab["tree_attention"] + ab["tree_accept"]
+        plan = self.ts.tree_attention_plan(self.step.d["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix,
+                                           workloads.BLOCK_SIZE)
+        return {
+            "ms_per_step": round(ms, 5), "ms_per_step_median": round(statistics.median(t["step"]), 5),
+            "ms_per_step_min": round(min(t["step"]), 5),
+            "value": round(ab["step"] / (ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+            "pct_of_hbm_peak": round(100 * ab["step"] / (ms * 1e-3) / 1e9 / peak, 2),
+            "nodes_verified_per_s": round(w.B * w.m / (ms * 1e-3), 1),
+            "nodes_verified_per_s_attention_accept": round(w.B * w.m / ((attn + acc) * 1e-3), 1),
+            "kernels_ms": {"tree_build": round(t_b, 5), "tree_attention": round(attn, 5),
+                           "tree_accept": round(acc, 5)},
+            "kernels_tbs": {"tree_build": round(ab["tree_build"] / (t_b * 1e-3) / 1e12, 4),
+                            "tree_attention": round(ab["tree_attention"] / (attn * 1e-3) / 1e12, 4),
+                            "tree_accept": round(ab["tree_accept"] / (acc * 1e-3) / 1e12, 4)},
+            "attention_ms_isolated": round(mean(t["attn"]), 5),
+            "attention_accept_pct_of_hbm_peak": round(100 * aa_bytes / ((attn + acc) * 1e-3) / 1e9 / peak, 2),
+            "attention_tflops": round(self.flops / (attn * 1e-3) / 1e12, 2),
+            "attention_frac_of_binding_roof": round(t_roof / (attn * 1e-3), 4),
+            "algorithmic_bytes": ab, "attention_flops": int(self.flops),
+            "attention_plan": plan, "roofline": roof,
+        }
+
+    def free(self):
+        self.graphs = None
+        self.step = None
+
+
+def time_cases(cases, args, flush, stream, world):
+    """The timed region: barrier + synchronize on both sides of K replays per case."""
+    barrier(world)
+    torch.cuda.synchronize()
+    for c in cases:
+        c.time_steps(args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+
+
+def next_rows_for(case, args, flush, stream, dev, with_oracle):
+    step, w = case.step, case.w
+    return {"kv_commit": run_kv_commit(step, w, args, flush, stream, with_oracle),
+            "lm_head_argmax": run_lm_head(w, args, flush, stream, dev, with_oracle),
+            "efficient_head": run_efficient_head(w, args, flush, stream, dev, with_oracle),
+            "accept_sample": run_accept_sample(step, w, args, flush, stream, with_oracle),
+            "tree_prune": run_tree_prune(step, w, args, flush, stream, with_oracle)}
 
 
 def run_ours(args, rank, world, dev):
@@ -251,177 +451,157 @@ def run_ours(args, rank, world, dev):
     from speculative_decoding_tree_eagle_gb300 import build as tsbuild
     tsbuild.build()
     ts.library()
-    w = get_workload(args)
-    inp = workloads.generate(w)
-    step = Step(w, inp, dev)
-    if w.plant_frac > 0:
-        # the planting recipe needs the draft tree: take it from this library's own tree_build
-        step.build()
-        torch.cuda.synchronize()
-        inp["logits"] = workloads.plant_paths(w, inp["logits"], step.tree["tokens"].cpu(),
-                                              step.tree["parents"].cpu())
-        step.d["logits"].copy_(inp["logits"])
+    name = args.workload
+    wl = workload_list(name, args.prefix)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        flush.zero_()
-        step.run()
-    torch.cuda.synchronize()
-    ts.check_status(step.status)
-    ops = [step.build, step.attention, step.accept]
-    per_step_launches = None
-    step_op = step.run
-    if not args.no_graph:
-        # one CUDA graph for the whole step (the timed number: the kernels of the three
-        # operations follow each other with programmatic dependent launch, as a caller's stream
-        # would run them), and one graph per operation for the per-operation breakdown; both keep
-        # host-side launch overhead (Python binding, argument checks) out of the device timeline
-        n0 = ts.launch_count()
-        g_step = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_step):
-            step.run()
-        per_step_launches = ts.launch_count() - n0
-        graphs = []
-        for op in ops:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                op()
-            graphs.append(g)
-        ops = [g.replay for g in graphs]
-        step_op = g_step.replay
-        for _ in range(2):
-            step_op()
-            for op in ops:
-                op()
-        torch.cuda.synchronize()
+    hbm, tensor = hbm_peak(), tensor_peak()
+    oracle_here = not args.no_cpu_baseline and world == 1 and rank == 0
 
+    # ---- the headline workload: every tree of it resident, graphs captured, then timed ----
+    cases = [Case(w, args, dev, flush) for w in wl]
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     t_wall0 = time.time()
-    # timed region: K whole steps, L2 flushed before each
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    n0 = ts.launch_count()
-    for i in range(args.steps):
-        flush.zero_()
-        evs[i][0].record(stream)
-        step_op()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    launches = ts.launch_count() - n0 if per_step_launches is None else per_step_launches * args.steps
-    barrier(world)
-    # per-operation breakdown: the same K steps again, events between the operations.  With
-    # graphs, the events are recorded inside one graph of the three operations (event-record
-    # nodes between their kernels), so each time is that operation's own kernels and not the
-    # device-side launch of a separate graph; without them (or without graph events in torch),
-    # events go between the launches.
-    op_times = []
-    in_graph = False
-    if not args.no_graph:
-        try:
-            ge = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-            g_ops = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_ops):
-                ge[0].record()
-                step.build()
-                ge[1].record()
-                step.attention()
-                ge[2].record()
-                step.accept()
-                ge[3].record()
-            for _ in range(2):
-                g_ops.replay()
-            torch.cuda.synchronize()
-            for i in range(args.steps):
-                flush.zero_()
-                g_ops.replay()
-                torch.cuda.synchronize()
-                op_times.append([ge[j].elapsed_time(ge[j + 1]) for j in range(3)])
-            in_graph = True
-        except (TypeError, RuntimeError):
-            op_times = []
-    if not in_graph:
-        pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.zero_()
-            e = pevs[i]
-            e[0].record(stream)
-            ops[0]()
-            e[1].record(stream)
-            ops[1]()
-            e[2].record(stream)
-            ops[2]()
-            e[3].record(stream)
-        torch.cuda.synchronize()
-        op_times = [[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in pevs]
+    time_cases(cases, args, flush, stream, world)
     # keep the GPU busy for at least ~1.5 s overall so the clock sampler sees the load
     while time.time() - t_wall0 < 1.5:
         flush.zero_()
-        step_op()
+        cases[-1]._run("step")
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ts.check_status(step.status)
 
-    t_step = [e[0].elapsed_time(e[1]) for e in evs]
-    t_build = [t[0] for t in op_times]
-    t_attn = [t[1] for t in op_times]
-    t_acc = [t[2] for t in op_times]
-    total_ms = sum(t_step)
-    total_ms = allreduce_max(total_ms, world, dev)
-    ab = algo_bytes(w, inp["prefix_len"].tolist())
+    step_ms = [sum(c.t["step"][i] for c in cases) for i in range(args.steps)]
+    total_ms = allreduce_max(sum(step_ms), world, dev)
     ms = total_ms / args.steps
-    value = world * ab["step"] / (ms * 1e-3) / 1e12
-    peak, peak_kind = hbm_peak()
-    mean = lambda x: sum(x) / len(x)
-    attn_ms = mean(t_attn)
-    traffic = ncu_traffic(args.workload)
-    roofline = attention_roofline(ab["tree_attention"], attention_flops(w, inp["prefix_len"].tolist()), attn_ms,
-                                  (peak, peak_kind), tensor_peak(), traffic)
+    step_bytes = sum(c.ab["step"] for c in cases)
+    nodes = sum(c.w.B * c.w.m for c in cases)
+    value = world * step_bytes / (ms * 1e-3) / 1e12
+    per_case = {c.w.name: c.summary(hbm, tensor, ncu_traffic(c.w.name)) for c in cases}
+    attn_ms = sum(per_case[c.w.name]["kernels_ms"]["tree_attention"] for c in cases)
+    acc_ms = sum(per_case[c.w.name]["kernels_ms"]["tree_accept"] for c in cases)
+    attn_bytes = sum(c.ab["tree_attention"] for c in cases)
+    attn_flops = sum(c.flops for c in cases)
+    if len(cases) == 1:
+        roofline = dict(per_case[wl[0].name]["roofline"])
+    else:
+        # the sweep's attention against the HBM roof (the spec unit), with the fraction of
+        # the binding roofs beside it (sum over the trees of max(bytes/HBM, FLOPs/tensor) / time)
+        traffic = [ncu_traffic(c.w.name) for c in cases]
+        achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "tree_attention (tcgen05 kernel + split-K combine), all four trees",
+                    "achieved": round(achieved, 1), "peak": hbm[0], "peak_kind": hbm[1], "unit": "GB/s",
+                    "frac": round(achieved / hbm[0], 4),
+                    "traffic": sum(traffic) if all(x is not None for x in traffic) else None,
+                    "frac_of_binding_roofs": round(
+                        sum(roof_time_s(c.ab["tree_attention"], c.flops, hbm[0], tensor[0]) for c in cases)
+                        / (attn_ms * 1e-3), 4)}
+    launches = sum(c.step_launches for c in cases)
+    w0 = wl[0]
     res = {
         "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "ms_per_step_median": round(statistics.median(t_step), 5), "ms_per_step_min": round(min(t_step), 5),
+        "ms_per_step_median": round(statistics.median(step_ms), 5), "ms_per_step_min": round(min(step_ms), 5),
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
-                   "prefix": list(w.prefix), "tree_nodes": w.m, "top_k": w.k, "depth": w.depth, "vocab": w.V,
-                   "block_size": workloads.BLOCK_SIZE, "l2": "flushed (512 MB write) before every timed step",
-                   "launch": "API calls" if args.no_graph else
-                             ("one CUDA graph per step (per-operation times: events recorded inside one graph "
-                              "of the three operations)" if in_graph else
-                              "one CUDA graph per step (per-operation times: one graph per operation)"),
-                   "parallelism": f"replicas{world}"},
-        "pct_of_hbm_peak": round(100 * value * 1e3 / peak, 2),
-        "nodes_verified_per_s": round(world * w.B * w.m / (ms * 1e-3), 1),
-        "nodes_verified_per_s_attention_accept": round(world * w.B * w.m / ((attn_ms + mean(t_acc)) * 1e-3), 1),
-        "kernels_ms": {"tree_build": round(mean(t_build), 5), "tree_attention": round(attn_ms, 5),
-                       "tree_accept": round(mean(t_acc), 5)},
-        "kernels_tbs": {k: round(ab[k] / (mean(t) * 1e-3) / 1e12, 4) for k, t in
-                        (("tree_build", t_build), ("tree_attention", t_attn), ("tree_accept", t_acc))},
-        "algorithmic_bytes": ab,
-        "attention_tflops": round(attention_flops(w, inp["prefix_len"].tolist()) / (attn_ms * 1e-3) / 1e12, 2),
-        "attention_plan": ts.tree_attention_plan(step.d["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix,
-                                                 workloads.BLOCK_SIZE),
+        "vs_baseline": None, "dtype": "bf16" if w0.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(name, args, world),
+        "pct_of_hbm_peak": round(100 * value * 1e3 / hbm[0], 2),
+        "nodes_verified_per_s": round(world * nodes / (ms * 1e-3), 1),
+        "nodes_verified_per_s_attention_accept": round(world * nodes / ((attn_ms + acc_ms) * 1e-3), 1),
+        "attention_accept_pct_of_hbm_peak": round(
+            100 * (attn_bytes + sum(c.ab["tree_accept"] for c in cases)) / ((attn_ms + acc_ms) * 1e-3) / 1e9
+            / hbm[0], 2),
+        "kernels_ms": {k: round(sum(per_case[c.w.name]["kernels_ms"][k] for c in cases), 5)
+                       for k in ("tree_build", "tree_attention", "tree_accept")},
+        "kernels_ms_method": "marginal (sums to the step): t(build), t(build+attention) - t(build), "
+                             "t(step) - t(build+attention), each a CUDA graph replayed after an L2 flush",
+        "algorithmic_bytes": {k: sum(c.ab[k] for c in cases) for k in ("tree_build", "tree_attention",
+                                                                       "tree_accept", "step")},
+        "attention_tflops": round(attn_flops / (attn_ms * 1e-3) / 1e12, 2),
         "clocks": clocks,
         "gpu_launches": int(launches),
         "roofline": roofline,
     }
-    res["next_rows"] = {"kv_commit": run_kv_commit(step, w, args, flush, stream, world),
-                        "lm_head_argmax": run_lm_head(w, args, flush, stream, dev),
-                        "efficient_head": run_efficient_head(w, args, flush, stream, dev),
-                        "accept_sample": run_accept_sample(step, w, args, flush, stream, world),
-                        "tree_prune": run_tree_prune(step, w, args, flush, stream)}
     if not args.no_e2e:
-        res["e2e"] = run_e2e(step, w, ab, args, dev, world)
-    return res, w, inp
+        res["e2e"] = run_e2e(cases, args, dev, world)
+    if oracle_here:
+        res["cpu_baseline"] = cpu_baseline(wl, [c.inp for c in cases], budget_s=12.0, single_thread_of=name,
+                                           args=args)
+    per_config = {}
+    for c in cases:
+        e = per_case[c.w.name]
+        if oracle_here:
+            e["cpu_baseline"] = cpu_baseline([c.w], [c.inp], budget_s=2.0)
+        per_config[c.w.name] = e
+    if len(cases) == 1 and not args.no_next_rows:
+        res["next_rows"] = next_rows_for(cases[0], args, flush, stream, dev, oracle_here)
+    for c in cases:
+        c.free()
+    del cases
+    torch.cuda.empty_cache()
+
+    # ---- the other configurations, one at a time ----
+    if not args.no_per_config and name in SWEEPS:
+        for cname in OTHER_CONFIGS:
+            w = workload_list(cname, args.prefix)[0]
+            c = Case(w, args, dev, flush)
+            time_cases([c], args, flush, stream, world)
+            e = c.summary(hbm, tensor, ncu_traffic(w.name))
+            if oracle_here:
+                e["cpu_baseline"] = cpu_baseline([w], [c.inp], budget_s=2.0)
+            if not args.no_next_rows:
+                e["next_rows"] = next_rows_for(c, args, flush, stream, dev, oracle_here and cname == "llama2_7b")
+            per_config[w.name] = e
+            c.free()
+            del c
+            torch.cuda.empty_cache()
+    res["per_config"] = per_config
+    return res
+
+
+def run_e2e(cases, args, dev, world):
+    """The same metric through the public API with host buffers: every step copies each tree's
+    inputs from pinned host memory, runs the three calls and reads the tree and the
+    acceptance result back."""
+    names = ["draft_logp", "root_tokens", "q", "k_cache", "v_cache", "block_table", "prefix_len", "logits"]
+    hosts, outs, h_outs = [], [], []
+    for c in cases:
+        step = c.step
+        hosts.append({n: step.host[n].pin_memory() for n in names})
+        o = {"tokens": step.tree["tokens"], "parents": step.tree["parents"], "accept_len": step.acc["accept_len"],
+             "accept_path": step.acc["accept_path"], "bonus": step.acc["bonus"]}
+        outs.append(o)
+        h_outs.append({n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in o.items()})
+    h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for c, host, o, ho in zip(cases, hosts, outs, h_outs):
+            for n in names:
+                c.step.d[n].copy_(host[n], non_blocking=True)
+            c.step.run()
+            for n, t in o.items():
+                ho[n].copy_(t, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            times.append(a.elapsed_time(b))
+    total = allreduce_max(sum(times), world, dev)
+    ms = total / args.steps
+    step_bytes = sum(c.ab["step"] for c in cases)
+    del hosts, h_outs
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e12, 4), "unit": "TB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
 # hidden size of the target model each workload is shaped after (the LM head is [V, d_model])
 D_MODEL = {"llama2_7b": 4096, "llama3_8b_gqa": 4096, "llama2_70b_gqa": 8192}
 
 
-def run_lm_head(w, args, flush, stream, dev):
+def run_lm_head(w, args, flush, stream, dev, with_oracle):
     """The target LM head with the per-row argmax fused into its GEMM (the row after the hot
     path): hidden [B*m, d_model] x weight [V, d_model]^T, seeded Gaussian bf16 weights, K calls,
     L2 flushed before each."""
@@ -465,7 +645,7 @@ def run_lm_head(w, args, flush, stream, dev):
     res = {"ms": round(ms, 5), "shape": {"rows": M, "vocab": V, "d_model": K}, "algorithmic_bytes": int(byts),
            "tb_s": round(tb_s, 4), "tflops": round(tflops, 2), "bound": bound, "frac_of_measured_peak": round(frac, 4),
            "logits_bytes_not_written": int(M * V * 4)}
-    if not args.no_cpu_baseline and _WORLD == 1:
+    if with_oracle:
         # the oracle beside it: fp64 logits and argmax of a bounded sample of rows, scaled to all rows
         import oracle
         n = min(M, 8)
@@ -478,7 +658,7 @@ def run_lm_head(w, args, flush, stream, dev):
     return res
 
 
-def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, k_tile=2):
+def run_efficient_head(w, args, flush, stream, dev, with_oracle, rank=256, tile_tokens=1024, k_tile=2):
     """One draft step of the two-stage efficient head (the row after the hot path): the B*k
     frontier rows of a drafter with a d_model-wide hidden state, seeded Gaussian bf16 factors;
     rank, tile size and candidates per tile are a reading (the page states none)."""
@@ -513,7 +693,7 @@ def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, 
                                          "k_tile": k_tile, "candidates": C, "k": k},
            "algorithmic_bytes": int(byts), "tb_s": round(byts / (ms * 1e-3) / 1e12, 4),
            "full_head_bytes": int(full_head), "bound": "hbm (low-rank head + gathered candidate rows)"}
-    if not args.no_cpu_baseline and _WORLD == 1:
+    if with_oracle:
         import oracle
         n = min(M, 2)
         t0 = time.perf_counter()
@@ -524,7 +704,7 @@ def run_efficient_head(w, args, flush, stream, dev, rank=256, tile_tokens=1024, 
     return res
 
 
-def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
+def run_accept_sample(step, w, args, flush, stream, with_oracle, temperature=1.0):
     """Verification at T > 0 by multi-round rejection sampling (the row after greedy
     acceptance), both proposal modes, on the step's own tree.  Target logits: the step's
     N(0,1) logits with one child of every expanded node raised to ln(V) + U(0, 4) (kept with
@@ -581,7 +761,7 @@ def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
         r = {"ms": round(ms, 5), "mean_accept_len": round(float(alen.mean()), 3),
              "bytes_min": byts, "gb_s": round(byts / (ms * 1e-3) / 1e9, 1),
              "bound": "latency (one CTA per sequence walks the tree; a few row passes per level)"}
-        if not args.no_cpu_baseline and world == 1:
+        if with_oracle:
             import oracle
             lh = logits.float().cpu().numpy()
             dh = d["draft_logp"].cpu().numpy() if mode == "draft" else None
@@ -595,7 +775,7 @@ def run_accept_sample(step, w, args, flush, stream, world, temperature=1.0):
     return res
 
 
-def run_tree_prune(step, w, args, flush, stream, costs=(1.0, 10.0, 0.05)):
+def run_tree_prune(step, w, args, flush, stream, with_oracle, costs=(1.0, 10.0, 0.05)):
     """Cost-aware pruning of the step's tree before verification (the harness row): three
     launches, no host sync inside the events; the cost model (t_draft, t_fixed, t_node) is an
     illustrative one in arbitrary units."""
@@ -621,7 +801,7 @@ def run_tree_prune(step, w, args, flush, stream, costs=(1.0, 10.0, 0.05)):
     byts = B * m * (4 * 4 + 8) + B * n * (4 * 5 + 8 + 8 * W) + B * 4
     res = {"ms": round(ms, 5), "costs": list(costs), "n": n, "algorithmic_bytes": int(byts),
            "bound": "latency (three small launches)"}
-    if not args.no_cpu_baseline and _WORLD == 1:
+    if with_oracle:
         import oracle
         hh = {k: v.cpu().numpy() for k, v in tree.items()}
         t0 = time.perf_counter()
@@ -630,7 +810,7 @@ def run_tree_prune(step, w, args, flush, stream, costs=(1.0, 10.0, 0.05)):
     return res
 
 
-def run_kv_commit(step, w, args, flush, stream, world):
+def run_kv_commit(step, w, args, flush, stream, with_oracle):
     """The KV commit of the step's accepted paths (the row after the hot path): K calls on
     the step's own accept outputs, block table and prefix lengths restored before each call
     (outside the events), L2 flushed."""
@@ -667,7 +847,7 @@ def run_kv_commit(step, w, args, flush, stream, world):
     res = {"ms": round(ms, 5), "accepted_rows": int(sum(al)), "moved_rows": int(moved),
            "algorithmic_bytes": int(byts), "bound": "latency (a few rows per sequence; one CTA each)"}
     cache_bytes = d["k_cache"].numel() * d["k_cache"].element_size() * 2
-    if not args.no_cpu_baseline and world == 1 and cache_bytes <= (256 << 20):
+    if with_oracle and cache_bytes <= (256 << 20):
         # the oracle beside it (cpu-baseline leg): same caches, table, lengths and paths
         import oracle
         view = (lambda t: t.cpu().view(torch.int16).numpy()) if w.dtype == "bf16" else (lambda t: t.cpu().numpy())
@@ -683,105 +863,107 @@ def run_kv_commit(step, w, args, flush, stream, world):
     return res
 
 
-def run_e2e(step, w, ab, args, dev, world):
-    """Same metric through the public API with host buffers: every step copies its inputs
-    from pinned host memory and reads the tree + acceptance result back."""
-    names = ["draft_logp", "root_tokens", "q", "k_cache", "v_cache", "block_table", "prefix_len", "logits"]
-    host = {n: step.host[n].pin_memory() for n in names}
-    outs = {"tokens": step.tree["tokens"], "parents": step.tree["parents"], "accept_len": step.acc["accept_len"],
-            "accept_path": step.acc["accept_path"], "bonus": step.acc["bonus"]}
-    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
-    stream = torch.cuda.current_stream()
-    times = []
-    for i in range(args.warmup + args.steps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for n in names:
-            step.d[n].copy_(host[n], non_blocking=True)
-        step.run()
-        for n, t in outs.items():
-            host_out[n].copy_(t, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        if i >= args.warmup:
-            times.append(a.elapsed_time(b))
-    total = allreduce_max(sum(times), world, dev)
-    ms = total / args.steps
-    return {"value": round(world * ab["step"] / (ms * 1e-3) / 1e12, 4), "unit": "TB/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-
-
 # ------------------------------------------------------------------------------------
 # CPU oracle (reported baseline / reference arm)
 # ------------------------------------------------------------------------------------
-def oracle_sample_step(w, inp, heads):
-    """One bounded sample of the step on the fp64 oracle: the whole tree_build and
-    tree_accept, and tree_attention for ``heads`` query heads of every sequence."""
+def oracle_sample(w, inp, heads):
+    """One bounded sample of a verify step on the fp64 oracle: sequence 0 only, its whole
+    tree_build and tree_accept, and tree_attention for ``heads`` query heads of it (every
+    node).  Returns the sample's algorithmic bytes (the unit the metric is scaled by)."""
     import oracle
-    tr = oracle.tree_build(inp["draft_logp"].numpy(), inp["root_tokens"].numpy(), w.k, w.depth, w.m)
-    sel = [(b, i, h) for b in range(w.B) for i in range(w.m) for h in heads]
-    oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
-                          inp["prefix_len"].numpy(), tr["mask"], 1.0 / math.sqrt(w.d), select=sel)
-    amax = oracle.target_argmax(inp["logits"])
+    tr = oracle.tree_build(inp["draft_logp"][:1].numpy(), inp["root_tokens"][:1].numpy(), w.k, w.depth, w.m)
+    sel = [(0, i, h) for i in range(w.m) for h in heads]
+    oracle.tree_attention(inp["q"][:1], inp["k_cache"], inp["v_cache"], inp["block_table"][:1].numpy(),
+                          inp["prefix_len"][:1].numpy(), tr["mask"], 1.0 / math.sqrt(w.d), select=sel)
+    amax = oracle.target_argmax(inp["logits"][:1])
     oracle.accept_longest_path(tr["tokens"], tr["parents"], amax)
 
 
-def oracle_sample_bytes(w, ab, heads):
-    frac = len(heads) / w.Hq
-    return ab["tree_build"] + ab["tree_attention"] * frac + ab["tree_accept"]
+def oracle_sample_bytes(w, inp, heads):
+    w1 = dataclasses.replace(w, B=1)
+    ab = algo_bytes(w1, inp["prefix_len"][:1].tolist())
+    return ab["tree_build"] + ab["tree_attention"] * len(heads) / w.Hq + ab["tree_accept"]
 
 
-def pick_heads(w):
-    g = w.Hq // w.Hkv
-    n = max(1, min(w.Hq, 4))
-    return [h * g % w.Hq for h in range(n)] if g > 1 else list(range(n))
+def sample_heads(w):
+    # query head 0 (every node of sequence 0): a sweep step of the oracle stays near 4 s
+    return [0]
 
 
-def cpu_baseline(w, inp, budget_s=12.0):
-    ab = algo_bytes(w, inp["prefix_len"].tolist())
-    heads = pick_heads(w)
+def _sample_desc(ws, reps, dt, threads):
+    parts = ", ".join(f"{w.name}: {len(sample_heads(w))} of {w.Hq} query heads" for w in ws)
+    return (f"fp64 numpy oracle on sequence 0 of each batch: its whole tree_build and tree_accept, "
+            f"tree_attention for every node of one query head ({parts}); {reps} repetitions of "
+            f"{dt:.3f} s; metric scaled by the sample's algorithmic bytes; numpy's BLAS on {threads} "
+            f"thread(s) (the attention products), the tree passes single-threaded")
+
+
+def oracle_rate(ws, inps, budget_s):
+    """Repeat the sample over all workloads of ``ws`` until ``budget_s`` is spent: (bytes/s, reps, s/rep)."""
+    byts = sum(oracle_sample_bytes(w, inp, sample_heads(w)) for w, inp in zip(ws, inps))
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle_sample_step(w, inp, heads)
+        for w, inp in zip(ws, inps):
+            oracle_sample(w, inp, sample_heads(w))
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = (time.perf_counter() - t0) / n
-    byts = oracle_sample_bytes(w, ab, heads)
-    return {"value": round(byts / dt / 1e12, 8), "unit": "TB/s", "cores": _CORES, "kind": "oracle",
-            "sample": f"fp64 numpy oracle: full tree_build + tree_accept, tree_attention for {len(heads)} of "
-                      f"{w.Hq} query heads (all sequences and nodes); {n} repetitions, {dt:.3f} s each; "
-                      f"metric scaled by the sample's algorithmic bytes; numpy's BLAS may use all {_CORES} "
-                      f"threads (the attention products), the tree passes run single-threaded"}
+    return byts / dt, n, dt
+
+
+def cpu_baseline(ws, inps, budget_s, single_thread_of=None, args=None):
+    """The oracle as it stands on this host: all cores; with ``single_thread_of`` also the same
+    sample on one thread (a child process with one BLAS thread)."""
+    rate, n, dt = oracle_rate(ws, inps, budget_s)
+    res = {"value": round(rate / 1e12, 8), "unit": "TB/s", "cores": _ORACLE_THREADS, "kind": "oracle",
+           "sample": _sample_desc(ws, n, dt, _ORACLE_THREADS)}
+    if single_thread_of is not None:
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-child", single_thread_of,
+               "--oracle-budget", str(budget_s)]
+        if args is not None and args.prefix is not None:
+            cmd += ["--prefix", str(args.prefix)]
+        try:
+            r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
+            line = [l for l in r.stdout.splitlines() if l.startswith("{")][-1]
+            one = json.loads(line)
+            res["single_thread"] = {"value": one["value"], "unit": "TB/s", "cores": 1, "sample": one["sample"]}
+        except Exception as e:  # reported, not fatal: the GPU line stands without it
+            res["single_thread"] = {"value": None, "error": f"{type(e).__name__}: {e}"[:200]}
+    return res
+
+
+def oracle_child(args):
+    ws = workload_list(args.oracle_child, args.prefix)
+    inps = [workloads.generate(w) for w in ws]
+    rate, n, dt = oracle_rate(ws, inps, args.oracle_budget or 10.0)
+    print(json.dumps({"value": round(rate / 1e12, 8), "sample": _sample_desc(ws, n, dt, _ORACLE_THREADS)}),
+          flush=True)
 
 
 def run_reference(args, rank, world):
-    w = get_workload(args)
-    inp = workloads.generate(w)
-    ab = algo_bytes(w, inp["prefix_len"].tolist())
-    heads = pick_heads(w)
+    ws = workload_list(args.workload, args.prefix)
+    inps = [workloads.generate(w) for w in ws]
+    byts = sum(oracle_sample_bytes(w, inp, sample_heads(w)) for w, inp in zip(ws, inps))
     for _ in range(args.warmup):
-        oracle_sample_step(w, inp, heads)
+        for w, inp in zip(ws, inps):
+            oracle_sample(w, inp, sample_heads(w))
     ts_ = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_sample_step(w, inp, heads)
+        for w, inp in zip(ws, inps):
+            oracle_sample(w, inp, sample_heads(w))
         ts_.append(time.perf_counter() - t0)
     ms = 1e3 * sum(ts_) / len(ts_)
-    byts = oracle_sample_bytes(w, ab, heads)
     value = byts / (ms * 1e-3) / 1e12
-    sample = (f"fp64 numpy oracle: full tree_build + tree_accept, tree_attention for {len(heads)} of {w.Hq} "
-              f"query heads; metric scaled by the sample's algorithmic bytes; numpy's BLAS may use all "
-              f"{_CORES} threads (the attention products), the tree passes run single-threaded")
+    sample = _sample_desc(ws, len(ts_), ms / 1e3, _ORACLE_THREADS)
     return {"impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "TB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
-                       "prefix": list(w.prefix), "tree_nodes": w.m, "vocab": w.V},
-            "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": _CORES, "kind": "oracle",
+            "config": config_of(args.workload, args, world),
+            "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": _ORACLE_THREADS, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 8), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -825,6 +1007,9 @@ def allreduce_max(x, world, dev):
 
 def main():
     args = parse()
+    if args.oracle_child is not None:
+        oracle_child(args)
+        return
     if args.impl == "reference":
         # the oracle arm uses no GPU and no collective: rank 0 alone runs it, the other
         # ranks leave at once (no process group is formed)
@@ -835,10 +1020,8 @@ def main():
     rank, world, local = init_dist(args)
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    res, w, inp = run_ours(args, rank, world, dev)
+    res = run_ours(args, rank, world, dev)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
-            res["cpu_baseline"] = cpu_baseline(w, inp)
         print(json.dumps(res), flush=True)
     if world > 1 and _PG is not None:
         _PG.destroy_process_group()
