@@ -188,7 +188,7 @@ def tree_attention_plan(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: int, d
     out = (ctypes.c_int * 5)()
     _check(library().ts_tree_attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, out))
     modes = {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}
-    return {"path": "tensor-core" if out[0] else "cuda-core", "m_tiles": out[1], "chunks": out[2],
+    return {"path": "tensor-core" if out[0] else "cuda-core", "row_groups": out[1], "chunks": out[2],
             "tiles_per_chunk": out[3], "split": modes.get(out[4], str(out[4]))}
 
 

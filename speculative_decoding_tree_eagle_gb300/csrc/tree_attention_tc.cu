@@ -5,32 +5,35 @@
 // "lesty.tech — EAGLE-2 vs. Medusa", section 5 (the tree mask stays on chip, no global
 // re-reads) and section 8 (tree K/V sit in the same paged sequence after the prefix).
 //
-// Work unit: (sequence b, KV head, row group, chunk of 64-key tiles).  The g query heads
+// Work unit: (sequence b, KV head, row group, chunk of 128-key tiles).  The g query heads
 // that share a KV head and the m tree nodes are packed into GEMM rows, row = node*g +
-// head-in-group, so every K/V byte fetched from HBM serves m*g query rows on the tensor
-// cores.  A row group is one (NM = 1) or two (NM = 2) 128-row M tiles.  One CTA per SM.
+// head-in-group, so every K/V byte fetched serves up to 128 query rows on the tensor cores;
+// row groups past the first (m*g > 128) read the same K/V tiles, adjacent in launch order so
+// the second read comes from L2.  One CTA per SM.
 //
-// Warp roles (4 + 4*NM warps, then the extra producer warps; 288 threads for NM = 1, 384 for 2):
-//   warps 0,2,3 and the warps after the softmax warps
-//               warp 0 stages the chunk's physical block ids in shared memory; then one
-//               thread per producer warp issues TMA loads (K: warps 0 and 3; V: warp 2 and,
-//               for one-tile groups, the last warp; each an even share of every tile's
-//               boxes): per 64-key tile one box of min(block_size,64) rows x 64 bf16
-//               (128-byte swizzle) per page and head-dim half; positions past the sequence
-//               load an out-of-range block (zero fill).  STAGES-deep ring; each full barrier
-//               expects every producer of its operand.
-//   warp 1      TMEM allocator + the single thread that issues tcgen05.mma:
-//                 S_i = Q_i K^T     (M=128, N=64, K=128; A, B from shared memory)
-//                 O_i += P_i V      (M=128, N=128, K=64; A = P from TMEM, B = V MN-major)
-//   warps 4..   softmax, one thread per row (TMEM lane): load S, apply the tree mask on the
-//               tiles that reach the tree, online softmax in the log2 domain with lazy
-//               rescaling of O (only when the running max grows by more than 2^8), write P
-//               as bf16 into TMEM; then the epilogue.
-// Overlap: with one M tile, S and P are double-buffered in TMEM (S = Q K^T of tile t+2 runs
-// while tile t's softmax runs); with two M tiles the MMAs of one tile run during the
-// other tile's softmax.  P never aliases S.
-// TMEM columns: O_i at 128*i; S_{i,s} at 128*NM + 64*(i*SB + s); P_{i,s} after the S
-// buffers, 32 columns each.
+// Warp roles (12 warps + extra producers):
+//   warps 0,3 (+ extra)  K producers; warp 0 first stages the chunk's physical block ids in
+//                        shared memory.  One thread per producer warp issues TMA loads: per
+//                        128-key tile one box of min(block_size,64) rows x 64 bf16 (128-byte
+//                        swizzle) per page and head-dim half, an even share of the tile's boxes
+//                        per producer; positions past the sequence load an out-of-range block
+//                        (zero fill).  K ring of SK stages, V ring of SV stages.
+//   warp 2 (+ extra)     V producers (same scheme on the V ring).
+//   warp 1               TMEM allocator + the single thread that issues tcgen05.mma:
+//                          S_t  = Q K_t^T    (M=128, N=128, K=128; A, B from shared memory)
+//                          O   += P_t V_t    (M=128, N=128, K=128; A = P from TMEM, B = V MN-major)
+//                        S and P are double-buffered: Q K^T of tile t+2 is issued right after
+//                        P V of tile t, so the tensor cores work while the softmax of tile t+1
+//                        runs.
+//   warps 4..11          softmax, two threads per row (TMEM lane): warps 4..7 take keys 0..63
+//                        of every tile, warps 8..11 keys 64..127.  Each loads its 64 scores,
+//                        applies the tree mask on the tiles that reach the tree, exchanges its
+//                        row maximum with its partner through shared memory, and runs the
+//                        online softmax in the log2 domain with lazy rescaling of its half of O
+//                        (only when the running max grows by more than 2^8), writing P as bf16
+//                        into TMEM; then the epilogue.  Only the warps that hold rows of this
+//                        group take part.
+// TMEM columns: O [0,128), S_0 [128,256), S_1 [256,384), P_0 [384,448), P_1 [448,512).
 // Split over chunks of one (sequence, KV head, row group):
 //   direct   one chunk: the epilogue writes O / l.
 //   cluster  the chunks are the CTAs of one thread-block cluster (<= 8): after a cluster
@@ -38,9 +41,9 @@
 //            memory of the CTA that owns those rows (distributed shared memory), and after a
 //            second barrier every owner merges its rows locally and writes the output: no
 //            partials in HBM and no second launch.
-// Chunks are balanced: chunk c of a sequence of T tiles covers [c*T/nc, (c+1)*T/nc).
 //   global   more chunks than a cluster holds: fp32 partials go to the workspace and
 //            combine_kernel merges them.
+// Chunks are balanced: chunk c of a sequence of T tiles covers [ceil(c*T/nc), ceil((c+1)*T/nc)).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -56,13 +59,13 @@
 namespace ts {
 namespace tc {
 
-constexpr int BN = 64;    // keys per tile
-constexpr int BM = 128;   // rows per M tile
+constexpr int BN = 128;   // keys per tile
+constexpr int BM = 128;   // rows per CTA
 constexpr int HD = 128;   // head dim
 constexpr uint32_t QHALF = BM * 128;   // 128 rows x 64 bf16 = 16 KB
 constexpr uint32_t QTILE = 2 * QHALF;  // both head-dim halves
-constexpr uint32_t KHALF = BN * 128;   // 64 keys x 64 bf16 = 8 KB
-constexpr uint32_t KTILE = 2 * KHALF;  // 16 KB
+constexpr uint32_t KHALF = BN * 128;   // 128 keys x 64 bf16 = 16 KB
+constexpr uint32_t KTILE = 2 * KHALF;  // 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxChunkBoxes = 2048;       // physical-block ids a CTA stages in shared memory
 constexpr int kMaxCluster = 8;
@@ -70,38 +73,39 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 enum Mode { kDirect = 0, kCluster = 1, kGlobal = 2 };
 
-template <int NM>
 struct Cfg {
-  static constexpr int SB = NM == 1 ? 2 : 1;  // S / P buffers per M tile
-  static constexpr int STAGES = NM == 1 ? 5 : 4;
-  // A TMA instruction holds its issuing thread for a while (~0.19 us for a page-sized box),
-  // so the boxes of a tile are spread over K_PRODUCERS + V_PRODUCERS warps.  Two-tile groups
-  // are bound by their MMAs (a tile takes ~1.7 us, ~142 cycles per tcgen05.mma, against
-  // ~0.8 us of box issue per producer warp) and keep a single V warp; more producer warps
-  // (up to four of each) measured no faster in either group.  Warps 0 and 3 issue K, warp 2
-  // V, and the warps after the softmax warps (from EXTRA_WARP on) the remaining V parts,
-  // then K parts.
-  static constexpr int K_PRODUCERS = 2;
-  static constexpr int V_PRODUCERS = NM == 1 ? 2 : 1;
-  static constexpr int EXTRA_WARP = 4 + 4 * NM;
+  static constexpr int SK = 3;  // K ring stages (K is consumed two tiles ahead of V)
+  static constexpr int SV = 2;  // V ring stages
+  // A TMA instruction keeps its issuing thread busy for on the order of 100 cycles, and a
+  // 128-key tile of 16-token pages is 16 boxes per operand, so each operand has several
+  // issuing warps.  Warps 0 and 3 issue K, warp 2 V; the warps after the softmax warps
+  // issue the remaining V parts, then the remaining K parts.
+  static constexpr int K_PRODUCERS = 4;
+  static constexpr int V_PRODUCERS = 2;
+  // softmax: two threads per row (warps 4..7 the first 64 keys of a tile, warps 8..11 the
+  // other 64; warp w reaches TMEM lanes 32*(w%4) .. +31), which exchange their row maxima
+  // through shared memory once per tile
+  static constexpr int EXTRA_WARP = 12;
   static constexpr int THREADS = 32 * (EXTRA_WARP + (K_PRODUCERS - 2) + (V_PRODUCERS - 1));
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 128 * NM;
-  static constexpr uint32_t COL_P = COL_S + 64 * NM * SB;
+  static constexpr uint32_t COL_S = 128;
+  static constexpr uint32_t COL_P = 384;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = NM * QTILE;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KTILE;
-  // full_k[ST] full_v[ST] empty_k[ST] empty_v[ST] s_full[NM*SB] p_full[NM*SB] o_ready[NM] o_final[NM]
-  // (p_full is per S buffer: with two buffers a fast softmax warp may reach tile t+1 while
-  // slower warps of its M tile still work on tile t, and their arrivals must not mix)
-  static constexpr int NBAR = 4 * STAGES + 2 * NM * SB + 2 * NM;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t OFF_K = QTILE;
+  static constexpr uint32_t OFF_V = OFF_K + SK * KTILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + SV * KTILE;
+  // full_k[SK] empty_k[SK] full_v[SV] empty_v[SV] s_full[2] p_full[2] o_ready o_final
+  // xchg[4 quadrants][2 parities] (p_full is per S buffer: a fast softmax warp may reach tile
+  // t+1 while slower warps still work on tile t, and their arrivals must not mix)
+  static constexpr int NBAR = 2 * SK + 2 * SV + 6 + 8;
+  static constexpr uint32_t OFF_XCH = OFF_BAR + NBAR * 8;         // [2 parities][2 halves][128 rows] fp32
+  static constexpr uint32_t OFF_MISC = OFF_XCH + 2 * 2 * BM * 4;
   static constexpr uint32_t OFF_ML = OFF_MISC + 16;            // (max, sum) per row, cluster merge
-  static constexpr uint32_t OFF_BLK = OFF_ML + NM * BM * 8;
+  static constexpr uint32_t OFF_BLK = OFF_ML + BM * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_BLK + 4 * kMaxChunkBoxes + 1024;  // + alignment slack
-  static_assert(COL_P + 32 * NM * SB <= TMEM_COLS, "TMEM budget");
-  static_assert(2 * STAGES * KTILE >= NM * BM * 512, "O rows must fit in the K/V ring for the merge");
+  static_assert(COL_P + 64 * 2 <= TMEM_COLS, "TMEM budget");
+  static_assert(SK * KTILE >= BM * 512, "O rows must fit in the K ring for the merge");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct Params {
@@ -133,13 +137,32 @@ __device__ __forceinline__ uint32_t orow_off(int R, int c) {
   return static_cast<uint32_t>(R) * 512u + (static_cast<uint32_t>(c ^ (R & 31)) << 4);
 }
 
-template <int NM>
-__global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
-    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const Params p) {
-  using C = Cfg<NM>;
-  constexpr int ST = C::STAGES;
-  constexpr int SB = C::SB;
+// Visibility of keys kb .. kb+63 for one row: the prefix keys (< L), then the row's ancestor
+// bits of the tree positions (key - L) the 64 keys cover; positions at or past m are never
+// visible.  `mw` are the row's mask words (m <= 256, so at most four).
+__device__ __forceinline__ uint64_t visible64(int kb, int L, int m, uint64_t mw0, uint64_t mw1, uint64_t mw2,
+                                              uint64_t mw3) {
+  const int pre = L - kb;  // prefix keys among these 64
+  if (pre >= 64) return ~0ull;
+  const int tt0 = pre > 0 ? 0 : -pre;  // first tree position
+  const int ntree = m - tt0;           // tree positions left from tt0
+  uint64_t tb = 0ull;
+  if (ntree > 0) {
+    const int q = tt0 >> 6, sh = tt0 & 63;
+    const uint64_t lo = q == 0 ? mw0 : q == 1 ? mw1 : q == 2 ? mw2 : q == 3 ? mw3 : 0ull;
+    const uint64_t hi = q == 0 ? mw1 : q == 1 ? mw2 : q == 2 ? mw3 : 0ull;
+    tb = sh == 0 ? lo : (lo >> sh) | (hi << (64 - sh));
+    if (ntree < 64) tb &= (1ull << ntree) - 1ull;
+  }
+  return pre > 0 ? (((1ull << pre) - 1ull) | (tb << pre)) : tb;
+}
+
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const Params p) {
+  using C = Cfg;
+  constexpr int SK = C::SK;
+  constexpr int SV = C::SV;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -165,38 +188,42 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   if (nt == 0 && p.mode != kCluster) return;  // (an idle CTA of a cluster still merges)
   // a sequence whose tiles all fall into one chunk is written directly also in the global mode
   const bool direct = p.mode == kDirect || (p.mode == kGlobal && min(T, p.nchunk) == 1);
-  const int R0 = rg * NM * BM;
-  const int rows_here = min(p.rows - R0, NM * BM);
-  const int nma = (rows_here + BM - 1) / BM;
+  const int R0 = rg * BM;
+  const int rows_here = min(p.rows - R0, BM);
+  const int nact = (rows_here + 31) / 32;  // softmax warps that hold rows of this group
 
   auto bar = [&](int idx) -> uint32_t { return sbase + C::OFF_BAR + 8u * idx; };
   auto full_k = [&](int s) { return bar(s); };
-  auto full_v = [&](int s) { return bar(ST + s); };
-  auto empty_k = [&](int s) { return bar(2 * ST + s); };
-  auto empty_v = [&](int s) { return bar(3 * ST + s); };
-  auto s_full = [&](int i, int sb) { return bar(4 * ST + i * SB + sb); };
-  auto p_full = [&](int i, int sb) { return bar(4 * ST + NM * SB + i * SB + sb); };
-  auto o_ready = [&](int i) { return bar(4 * ST + 2 * NM * SB + i); };
-  auto o_final = [&](int i) { return bar(4 * ST + 2 * NM * SB + NM + i); };
+  auto empty_k = [&](int s) { return bar(SK + s); };
+  auto full_v = [&](int s) { return bar(2 * SK + s); };
+  auto empty_v = [&](int s) { return bar(2 * SK + SV + s); };
+  auto s_full = [&](int sb) { return bar(2 * SK + 2 * SV + sb); };
+  auto p_full = [&](int sb) { return bar(2 * SK + 2 * SV + 2 + sb); };
+  const uint32_t o_ready = bar(2 * SK + 2 * SV + 4);
+  const uint32_t o_final = bar(2 * SK + 2 * SV + 5);
+  auto xchg_bar = [&](int q, int par) { return bar(2 * SK + 2 * SV + 6 + 2 * q + par); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + C::OFF_MISC + 4);
-  float2* s_ml = reinterpret_cast<float2*>(sptr + C::OFF_ML);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(full_k(s), C::K_PRODUCERS);  // each producer warp registers its own bytes
-      mbar_init(full_v(s), C::V_PRODUCERS);
       mbar_init(empty_k(s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(full_v(s), C::V_PRODUCERS);
       mbar_init(empty_v(s), 1);
     }
-    for (int i = 0; i < NM; ++i) {
-      for (int sb = 0; sb < SB; ++sb) {
-        mbar_init(s_full(i, sb), 1);
-        mbar_init(p_full(i, sb), 128);
-      }
-      mbar_init(o_ready(i), 1);
-      mbar_init(o_final(i), 1);
+    for (int sb = 0; sb < 2; ++sb) {
+      mbar_init(s_full(sb), 1);
+      mbar_init(p_full(sb), 64 * nact);
     }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(xchg_bar(q, 0), 64);
+      mbar_init(xchg_bar(q, 1), 64);
+    }
+    mbar_init(o_ready, 1);
+    mbar_init(o_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -207,15 +234,15 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   // Q rows of this row group -> shared memory in the 128-byte-swizzled K-major layout
   // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.  Loads
   // are issued in batches of 4 per thread so their latencies overlap.
-  for (int c0 = threadIdx.x; c0 < NM * BM * 16; c0 += 4 * C::THREADS) {
+  for (int c0 = threadIdx.x; c0 < BM * 16; c0 += 4 * C::THREADS) {
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * C::THREADS;
       const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
-      const int grow = R0 + row;
       v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (nt > 0 && c < NM * BM * 16 && grow < p.rows) {
+      if (nt > 0 && c < BM * 16 && row < rows_here) {
+        const int grow = R0 + row;
         const int node = grow / p.g, head = kvh * p.g + grow % p.g;
         const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
         v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + off));
@@ -224,17 +251,16 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * C::THREADS;
-      if (c >= NM * BM * 16) break;
+      if (c >= BM * 16) break;
       const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
-      const int i = row >> 7, r = row & 127;
-      *reinterpret_cast<uint4*>(sptr + C::OFF_Q + i * QTILE + h * QHALF + r * 128 + ((j ^ (r & 7)) << 4)) = v[u];
+      *reinterpret_cast<uint4*>(sptr + C::OFF_Q + h * QHALF + row * 128 + ((j ^ (row & 7)) << 4)) = v[u];
     }
   }
-  // Physical block of every TMA box of this chunk -> shared memory (warp 0, coalesced,
-  // 4 independent loads in flight per lane); out-of-range ids are reported and replaced by
-  // the out-of-bounds block, positions past the sequence get the out-of-bounds block too.
-  const int rpb = min(p.block_size, BN);
-  const int bpt = BN / rpb;
+  // Physical block of every TMA box row group of this chunk -> shared memory (warp 0,
+  // coalesced, 4 independent loads in flight per lane); out-of-range ids are reported and
+  // replaced by the out-of-bounds block, positions past the sequence get it too.
+  const int rpb = min(p.block_size, 64);  // rows per box
+  const int bpt = BN / rpb;               // box rows per tile
   int* s_blk = reinterpret_cast<int*>(sptr + C::OFF_BLK);
   if (warp == 0) {
     const int nbox = nt * bpt;
@@ -281,24 +307,38 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
       const int kv = (warp == 0 || warp == 3 || (e >= 0 && e >= C::V_PRODUCERS - 1)) ? 0 : 1;
       const int part = warp == 0 ? 0 : warp == 3 ? 1 : warp == 2 ? 0 : kv == 1 ? e + 1 : 2 + e - (C::V_PRODUCERS - 1);
       const int nparts = kv == 0 ? C::K_PRODUCERS : C::V_PRODUCERS;
+      const int ST = kv == 0 ? SK : SV;
       const void* map = kv == 0 ? static_cast<const void*>(&tmk) : static_cast<const void*>(&tmv);
-      const int nbox = 2 * bpt;                    // boxes per tile: pages x head-dim halves
+      // K: per box row j of the tile and head-dim half h one box of rpb rows x 128 B, placed
+      // at h*KHALF + j*rpb*128 (each half of the tile is one K-major operand of 128 keys).
+      // V: per box row j one box of both halves (rpb rows x 2 x 128 B, two-half tensor map),
+      // placed at j*rpb*256 as [half][rows]: a P V step of 16 keys reads one page.
+      const int nbox = kv == 0 ? 2 * bpt : bpt;
       const int b_begin = part * nbox / nparts, b_end = (part + 1) * nbox / nparts;
+      const uint32_t box_bytes = kv == 0 ? rpb * 128 : rpb * 256;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t % ST;
         const uint32_t ph = (t / ST) & 1;
-        const int key0 = (t0 + t) * BN;
         const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
         const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
         if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(fb, static_cast<uint32_t>(b_end - b_begin) * rpb * 128);
-        const uint32_t dst0 = sbase + (kv == 0 ? C::OFF_K : C::OFF_V) + s * KTILE;
-        for (int e = b_begin; e < b_end; ++e) {
-          const int j = e >> 1, h = e & 1;      // page j of the tile, head-dim half h
-          const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
-          const int rin = blk < p.num_blocks ? (key0 + j * rpb) % p.block_size : 0;
-          tma_load_4d(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk);
+        mbar_expect_tx(fb, static_cast<uint32_t>(b_end - b_begin) * box_bytes);
+        if (kv == 0) {
+          const uint32_t dst0 = sbase + C::OFF_K + s * KTILE;
+          for (int e2 = b_begin; e2 < b_end; ++e2) {
+            const int j = e2 >> 1, h = e2 & 1;
+            const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
+            const int rin = blk < p.num_blocks ? (j * rpb) & (p.block_size - 1) : 0;
+            tma_load_4d(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk);
+          }
+        } else {
+          const uint32_t dst0 = sbase + C::OFF_V + s * KTILE;
+          for (int j = b_begin; j < b_end; ++j) {
+            const int blk = s_blk[t * bpt + j];
+            const int rin = blk < p.num_blocks ? (j * rpb) & (p.block_size - 1) : 0;
+            tma_load_5d(dst0 + j * rpb * 256, map, fb, 0, rin, 0, kvh, blk);
+          }
         }
         issued = t + 1;
       }
@@ -313,75 +353,74 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idq = idesc_bf16_f32(128, BN, 0, 0);
       constexpr uint32_t idp = idesc_bf16_f32(128, HD, 0, 1);
-      auto tO = [&](int i) { return tmem + 128u * i; };
-      auto tS = [&](int i, int sb) { return tmem + C::COL_S + 64u * (i * SB + sb); };
-      auto tP = [&](int i, int sb) { return tmem + C::COL_P + 32u * (i * SB + sb); };
-      auto qk = [&](int i, int s, int sb) {
+      auto tS = [&](int sb) { return tmem + C::COL_S + 128u * sb; };
+      auto tP = [&](int sb) { return tmem + C::COL_P + 64u * sb; };
+      auto qk = [&](int sk, int sb) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t h = kk >> 2, ko = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + i * QTILE + h * QHALF + ko, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + s * KTILE + h * KHALF + ko, 16, 1024);
-          mma_ss(tS(i, sb), a, bd, idq, kk > 0 ? 1u : 0u);
+          const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + h * QHALF + ko, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + sk * KTILE + h * KHALF + ko, 16, 1024);
+          mma_ss(tS(sb), a, bd, idq, kk > 0 ? 1u : 0u);
         }
-        tc_commit(s_full(i, sb));
+        tc_commit(s_full(sb));
       };
-      auto pv = [&](int i, int s, int sb, bool first) {
+      // B = V keys 16kk .. 16kk+15, MN-major: 64 head-dim columns per 128-byte row, 8-key
+      // groups 1 KB apart (stride offset), the second head-dim half rpb*128 further (leading
+      // offset); the keys sit in box row (16kk)/rpb at row (16kk)%rpb.  Descriptors of stage 0;
+      // a stage adds KTILE (in 16-byte units) to the start address field.
+      uint64_t vdesc[BN / 16];
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // B = V tile, MN-major: 64 head-dim columns per 128-byte row, 8-key groups 1 KB
-          // apart (stride offset), the second head-dim half KHALF further (leading offset).
-          const uint64_t bd = sdesc_sw128(sbase + C::OFF_V + s * KTILE + kk * 2048, KHALF, 1024);
-          mma_ts(tO(i), tP(i, sb) + 8u * kk, bd, idp, (first && kk == 0) ? 0u : 1u);
-        }
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const int key = 16 * kk;
+        const uint32_t off = (key / rpb) * rpb * 256 + (key % rpb) * 128;
+        vdesc[kk] = sdesc_sw128(sbase + C::OFF_V + off, rpb * 128, 1024);
+      }
+      auto pv = [&](int sv, int sb, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem, tP(sb) + 8u * kk, vdesc[kk] + static_cast<uint64_t>(sv * (KTILE >> 4)), idp,
+                 (first && kk == 0) ? 0u : 1u);
       };
       bool mok = true;
-      for (int t = 0; mok && t < SB && t < nt; ++t) {
-        mok = mbar_wait(full_k(t % ST), (t / ST) & 1, abort_flag, p.status);
+      for (int t = 0; mok && t < 2 && t < nt; ++t) {
+        mok = mbar_wait(full_k(t % SK), (t / SK) & 1, abort_flag, p.status);
         if (!mok) break;
         tc_fence_after();
-        for (int i = 0; i < nma; ++i) qk(i, t % ST, t % SB);
-        tc_commit(empty_k(t % ST));
+        qk(t % SK, t & 1);
+        tc_commit(empty_k(t % SK));
       }
       for (int t = 0; mok && t < nt; ++t) {
-        const int s = t % ST;
-        mok = mbar_wait(full_v(s), (t / ST) & 1, abort_flag, p.status);
+        const int sv = t % SV;
+        mok = mbar_wait(full_v(sv), (t / SV) & 1, abort_flag, p.status);
+        if (!mok) break;
+        mok = mbar_wait(p_full(t & 1), (t >> 1) & 1, abort_flag, p.status);
         if (!mok) break;
         tc_fence_after();
-        const int tn = t + SB;
-        for (int i = 0; i < nma; ++i) {
-          mok = mbar_wait(p_full(i, t % SB), (t / SB) & 1, abort_flag, p.status);
+        pv(sv, t & 1, t == 0);
+        tc_commit(o_ready);
+        tc_commit(empty_v(sv));
+        const int tn = t + 2;
+        if (tn < nt) {
+          mok = mbar_wait(full_k(tn % SK), (tn / SK) & 1, abort_flag, p.status);
           if (!mok) break;
           tc_fence_after();
-          pv(i, s, t % SB, t == 0);
-          tc_commit(o_ready(i));
-          if (tn < nt) {
-            if (i == 0) {
-              mok = mbar_wait(full_k(tn % ST), (tn / ST) & 1, abort_flag, p.status);
-              if (!mok) break;
-              tc_fence_after();
-            }
-            qk(i, tn % ST, tn % SB);
-            if (i == nma - 1) tc_commit(empty_k(tn % ST));
-          }
+          qk(tn % SK, tn & 1);
+          tc_commit(empty_k(tn % SK));
         }
-        if (!mok) break;
-        tc_commit(empty_v(s));
       }
-      for (int i = 0; i < nma; ++i) tc_commit(o_final(i));
-      if (!mok) {
-        for (int i = 0; i < nma; ++i) drain_wait(o_final(i), 0);
-      }
+      tc_commit(o_final);
+      if (!mok) drain_wait(o_final, 0);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < C::EXTRA_WARP) {
     // ------------------------------ softmax ------------------------------
-    const int i = (warp - 4) >> 2;
-    const int q4 = warp & 3;
-    if (i < nma && nt > 0) {
+    const int q4 = warp & 3;        // TMEM lane quadrant: rows 32*q4 .. +31
+    const int hh = (warp - 4) >> 2; // keys 64*hh .. +63 of every tile, O columns 64*hh .. +63
+    if (q4 < nact && nt > 0) {
       const int r = q4 * 32 + lane;
-      const int grow = R0 + i * BM + r;
-      const bool valid = grow < p.rows;
+      const int grow = R0 + r;
+      const bool valid = r < rows_here;
       const int node = valid ? grow / p.g : 0;
       uint64_t mw0 = 0, mw1 = 0, mw2 = 0, mw3 = 0;
       if (valid) {
@@ -392,46 +431,52 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
         if (p.W > 3) mw3 = mrow[3];
       }
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-      const uint32_t tO = tmem + lane_off + 128u * i;
+      const uint32_t tO = tmem + lane_off + 64u * hh;
       const float sl2 = p.scale_log2;
+      float* xch = reinterpret_cast<float*>(sptr + C::OFF_XCH);
+      // the partner thread's value for exchange round `round` (both threads of a row take part
+      // in every round; rounds alternate between two buffers, each with its own barrier)
+      auto exchange = [&](int round, float v, float* other) -> bool {
+        const int par = round & 1;
+        xch[(par * 2 + hh) * BM + r] = v;
+        mbar_arrive(xchg_bar(q4, par));
+        if (!mbar_wait_warp(xchg_bar(q4, par), (round >> 1) & 1, abort_flag, p.status)) return false;
+        *other = xch[(par * 2 + (hh ^ 1)) * BM + r];
+        return true;
+      };
       for (int t = 0; t < nt; ++t) {
-        const int sb = t % SB;
-        const uint32_t tS = tmem + lane_off + C::COL_S + 64u * (i * SB + sb);
-        const uint32_t tP = tmem + lane_off + C::COL_P + 32u * (i * SB + sb);
-        ok = mbar_wait_warp(s_full(i, sb), (t / SB) & 1, abort_flag, p.status);
+        const int sb = t & 1;
+        const uint32_t tS = tmem + lane_off + C::COL_S + 128u * sb + 64u * hh;
+        const uint32_t tP = tmem + lane_off + C::COL_P + 64u * sb + 32u * hh;
+        ok = mbar_wait_warp(s_full(sb), (t >> 1) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        float s[BN];
+        const int key0 = (t0 + t) * BN;
+        float s[64];
         {
-          uint32_t u[BN];
+          uint32_t u[64];
           tmem_ld64(tS, u);
 #pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u[c]);
         }
-        const int key0 = (t0 + t) * BN;
-        float mx = -INFINITY;
         if (key0 + BN > L) {
-          // one visibility bit per column: the prefix columns, then this row's ancestor bits of
-          // the tree positions the tile covers (positions at or past m are never visible)
-          const int pre = L - key0;             // prefix columns in this tile (< 64)
-          const int tt0 = pre > 0 ? 0 : -pre;   // first tree position in this tile
-          const int q = tt0 >> 6, sh = tt0 & 63;
-          const uint64_t lo = q == 0 ? mw0 : q == 1 ? mw1 : q == 2 ? mw2 : q == 3 ? mw3 : 0ull;
-          const uint64_t hi = q == 0 ? mw1 : q == 1 ? mw2 : q == 2 ? mw3 : 0ull;
-          uint64_t tb = sh == 0 ? lo : (lo >> sh) | (hi << (64 - sh));
-          const int ntree = p.m - tt0;          // tree positions left from tt0
-          if (ntree < 64) tb &= ntree > 0 ? (1ull << ntree) - 1ull : 0ull;
-          const uint64_t vis = pre > 0 ? (((1ull << pre) - 1ull) | (tb << pre)) : tb;
+          // one visibility bit per column (prefix columns, then this row's ancestors)
+          const uint64_t vis = visible64(key0 + 64 * hh, L, p.m, mw0, mw1, mw2, mw3);
 #pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = ((vis >> c) & 1ull) ? s[c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) s[c] = ((vis >> c) & 1ull) ? s[c] : -INFINITY;
         }
-        {  // eight independent running maxima, then a tree
+        float mx;
+        {  // eight independent running maxima, then a tree; then the partner's half
           float m8[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) m8[c] = s[c];
 #pragma unroll
-          for (int c = 8; c < BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
           mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          float mo;
+          ok = exchange(t, mx, &mo);
+          if (!ok) break;
+          mx = fmaxf(mx, mo);
         }
         if (!valid) mx = -INFINITY;
         const float mt = mx * sl2;
@@ -446,24 +491,27 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
           m_ref = mt;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        uint32_t pk[32];
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = valid ? ex2_approx(fmaf(s[2 * c], sl2, -mu)) : 0.f;
-          const float p1 = valid ? ex2_approx(fmaf(s[2 * c + 1], sl2, -mu)) : 0.f;
-          rs4[c & 3] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = valid ? ex2_approx(fmaf(s[2 * c], sl2, -mu)) : 0.f;
+            const float p1 = valid ? ex2_approx(fmaf(s[2 * c + 1], sl2, -mu)) : 0.f;
+            rs4[c & 3] += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tP, pk);
+          l_sum += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         }
-        l_sum += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-        tmem_st32(tP, pk);
         if (__any_sync(0xffffffffu, resc)) {
-          // O must hold P V of tile t-1 before it is rescaled
-          ok = mbar_wait_warp(o_ready(i), (t - 1) & 1, abort_flag, p.status);
+          // O must hold P V of tile t-1 before it is rescaled (the partner warp rescales the
+          // other 64 columns of the same rows with the same factor)
+          ok = mbar_wait_warp(o_ready, (t - 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
             tmem_ld32(tO + 32u * cc, o);
 #pragma unroll
@@ -472,33 +520,38 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
           }
         }
         tmem_st_wait();
-        if (i == 0 && key0 + BN > nkeys) {
+        if (key0 + BN > nkeys) {
           // zero V rows past the end of the sequence (their P is 0, but the cache slots may
           // hold non-finite garbage and 0 * inf would poison O)
-          const int s_ = t % ST;
-          ok = mbar_wait_warp(full_v(s_), (t / ST) & 1, abort_flag, p.status);
+          const int sv = t % SV;
+          ok = mbar_wait_warp(full_v(sv), (t / SV) & 1, abort_flag, p.status);
           if (!ok) break;
           const int jv = nkeys - key0;
           const int nz = (BN - jv) * 16;
-          for (int c = q4 * 32 + lane; c < nz; c += 128) {
-            const int row = jv + (c >> 4), h = (c >> 3) & 1, j = c & 7;
-            *reinterpret_cast<uint4*>(sptr + C::OFF_V + s_ * KTILE + h * KHALF + row * 128 + j * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+          for (int c = (hh * nact + q4) * 32 + lane; c < nz; c += 64 * nact) {
+            const int key = jv + (c >> 4), h = (c >> 3) & 1, j = c & 7;
+            const int off = (key / rpb) * rpb * 256 + h * rpb * 128 + (key % rpb) * 128 + j * 16;
+            *reinterpret_cast<uint4*>(sptr + C::OFF_V + sv * KTILE + off) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
         }
         tc_fence_before();
-        mbar_arrive(p_full(i, sb));
+        mbar_arrive(p_full(sb));
       }
-      if (ok) ok = mbar_wait_warp(o_final(i), 0, abort_flag, p.status);
+      if (ok) {  // the row's sum over both halves
+        float lo;
+        ok = exchange(nt, l_sum, &lo);
+        if (ok) l_sum += lo;
+      }
+      if (ok) ok = mbar_wait_warp(o_final, 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
         const int head = kvh * p.g + (valid ? grow % p.g : 0);
         if (direct) {
           const float inv = (valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
-          __nv_bfloat16* dst = p.out + ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD;
+          __nv_bfloat16* dst = p.out + ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + 64 * hh;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
             tmem_ld32(tO + 32u * cc, o);
             if (valid) {
@@ -513,13 +566,13 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
               }
             }
           }
-          if (valid && p.lse != nullptr)
+          if (valid && hh == 0 && p.lse != nullptr)
             p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (m_ref + log2f(l_sum)) * kLn2;
         } else if (p.mode == kGlobal) {
           const long long prow = (static_cast<long long>(bk) * p.rows + grow) * p.nchunk + chunk;
-          float* dst = p.part_o + prow * HD;
+          float* dst = p.part_o + prow * HD + 64 * hh;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
             tmem_ld32(tO + 32u * cc, o);
             if (valid) {
@@ -530,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
                                 __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
             }
           }
-          if (valid) p.part_ml[prow] = make_float2(m_ref, l_sum);
+          if (valid && hh == 0) p.part_ml[prow] = make_float2(m_ref, l_sum);
         }
         // cluster mode: O stays in TMEM until every CTA of the cluster has left its loop
       }
@@ -540,34 +593,36 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
   if (p.mode == kCluster) {
     // Merge through distributed shared memory.  Rows of the row group are split evenly over
     // the cs CTAs ("owners"); slot (c, row) of an owner's receive area holds CTA c's partial.
-    // 1) barrier: every CTA has left its loop, so all K/V rings are idle and reusable;
+    // 1) barrier: every CTA has left its loop, so all K rings are idle and reusable;
     // 2) every CTA pushes its (max, sum) and fp32 O rows into the owners' rings with remote
     //    stores (no round trips); 3) barrier: all pushes are visible; 4) each owner merges
     //    its rows from local shared memory and writes the output.
     const int cs = p.nchunk;
     const int q = static_cast<int>(cluster_ctarank());
-    const int per = NM * BM / cs;  // cs divides 128
+    const int per = BM / cs;  // cs divides 128
     tc_fence_before();
     cluster_sync_all();
     if (warp >= 4 && warp < C::EXTRA_WARP) {
-      const int i = (warp - 4) >> 2;
-      const int Rl = i * BM + (warp & 3) * 32 + lane;
-      const bool have = ok && i < nma && nt > 0 && R0 + Rl < p.rows;
+      const int hh = (warp - 4) >> 2;
+      const int Rl = (warp & 3) * 32 + lane;
+      const bool have = ok && nt > 0 && Rl < rows_here;
       const int owner = Rl / per;
       const int slot = q * per + (Rl - owner * per);
-      const float2 ml = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
-      st_dsmem_f2(dsmem_addr(sbase + C::OFF_ML + 8u * slot, owner), ml);
+      if (hh == 0) {
+        const float2 ml = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+        st_dsmem_f2(dsmem_addr(sbase + C::OFF_ML + 8u * slot, owner), ml);
+      }
       if (__any_sync(0xffffffffu, have)) {  // tcgen05.ld is warp-wide
         tc_fence_after();
-        const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 128u * i;
+        const uint32_t tO = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64u * hh;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
           tmem_ld32(tO + 32u * cc, o);
           if (have) {
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              st_dsmem_u4(dsmem_addr(sbase + C::OFF_K + orow_off(slot, cc * 8 + v4), owner),
+              st_dsmem_u4(dsmem_addr(sbase + C::OFF_K + orow_off(slot, 16 * hh + cc * 8 + v4), owner),
                           make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]));
           }
         }
@@ -578,8 +633,8 @@ __global__ void __launch_bounds__(Cfg<NM>::THREADS, 1)
     const float2* ml_local = reinterpret_cast<const float2*>(sptr + C::OFF_ML);
     for (int rr = warp; rr < per; rr += C::THREADS / 32) {
       const int Rl = q * per + rr;
+      if (Rl >= rows_here) break;
       const int grow = R0 + Rl;
-      if (grow >= p.rows) break;
       float M = -INFINITY;
       float2 mls[kMaxCluster];
 #pragma unroll
@@ -675,19 +730,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     p.lse[(static_cast<long long>(b) * p.m + node) * p.Hq + head] = (M + log2f(Ls)) * kLn2;
 }
 
-template <int NM>
 static cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(tree_attn_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<NM>::SMEM_BYTES);
+    err = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   return err;
 }
 
 // How many clusters of `cs` CTAs (one per SM) the device runs at once; 0 if unknown.
-template <int NM>
 static int active_clusters(int cs) {
   static std::mutex mu;
   static int cache[kMaxCluster + 1] = {};
@@ -695,11 +747,11 @@ static int active_clusters(int cs) {
   std::lock_guard<std::mutex> lock(mu);
   if (done[cs]) return cache[cs];
   done[cs] = true;
-  if (set_smem_attr<NM>() != cudaSuccess) return 0;
+  if (set_smem_attr() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, cs, 1);
-  cfg.blockDim = dim3(Cfg<NM>::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<NM>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 1;
@@ -708,7 +760,7 @@ static int active_clusters(int cs) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tree_attn_tc_kernel<NM>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tree_attn_tc_kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -717,33 +769,46 @@ static int active_clusters(int cs) {
 }
 
 struct Plan {
-  int NM, rowgroups, nc, tpc, mode;
+  int rowgroups, nc, tpc, mode;
 };
 
-// Makespan model in 64-key-tile units: waves x (tiles per CTA + fixed cost per CTA) plus,
-// for the global mode, the partial write/read and the combine launch.
+// Makespan model (microseconds).  A CTA streams tpc tiles of 128 keys at the larger of its
+// own pipeline rate (tau_c per tile) and its share of the HBM bandwidth when `active` CTAs
+// stream at once (each K/V tile is 64 KB; row groups past the first read it from L2), plus a
+// fixed cost per CTA (set-up, pipeline fill and drain, epilogue) and the merge of the split.
+struct CostModel {
+  double tau_c, c0, hbm_bytes_per_us, cluster_merge, global_merge;
+};
+
+static double makespan(const CostModel& cm, long long units, int unit_groups, int tpc, long long waves,
+                       long long active, double merge) {
+  const double tau_h = 65536.0 * static_cast<double>(active) / static_cast<double>(unit_groups) / cm.hbm_bytes_per_us;
+  const double tau = cm.tau_c > tau_h ? cm.tau_c : tau_h;
+  (void)units;
+  return static_cast<double>(waves) * (tpc * tau + cm.c0) + merge;
+}
+
 static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms) {
   Plan pl;
   if (num_sms < 1) num_sms = 1;
   const int rows = m * (Hq / Hkv);
-  pl.NM = rows > BM ? 2 : 1;
-  pl.rowgroups = (rows + pl.NM * BM - 1) / (pl.NM * BM);
+  pl.rowgroups = (rows + BM - 1) / BM;
   const int T = (max_prefix + m + BN - 1) / BN;
   const long long units = static_cast<long long>(B) * Hkv * pl.rowgroups;
-  const int c0 = 3;
-  const int rows_cta = rows < pl.NM * BM ? rows : pl.NM * BM;
-  const int cglob = 4 + (rows_cta * 2 + BN - 1) / BN;
-  long long best = -1;
+  const CostModel cm{0.75, 2.5, 6.5e6, 1.5, 3.0};
+  double best = -1.0;
   pl.nc = 1;
   pl.tpc = T;
   pl.mode = kDirect;
-  const int max_nc = T < 4096 ? T : 4096;
+  const int max_nc = T < 1024 ? T : 1024;
   for (int nc = 1; nc <= max_nc; ++nc) {
     const int tpc = (T + nc - 1) / nc;
     if ((T + tpc - 1) / tpc != nc) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;  // box ids staged for the smallest pages
-    const long long waves = (units * nc + num_sms - 1) / num_sms;
-    const long long cost = waves * (tpc + c0) + (nc > 1 ? waves * cglob : 0);
+    const long long ctas = units * nc;
+    const long long waves = (ctas + num_sms - 1) / num_sms;
+    const long long active = ctas < num_sms ? ctas : num_sms;
+    const double cost = makespan(cm, units, pl.rowgroups, tpc, waves, active, nc > 1 ? cm.global_merge : 0.0);
     if (best < 0 || cost < best) {
       best = cost;
       pl.nc = nc;
@@ -764,8 +829,7 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
       }
     } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n) {
       const int tpc = (T + n - 1) / n;
-      const int act = pl.NM == 1 ? active_clusters<1>(n) : active_clusters<2>(n);
-      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && act > 0) {
+      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && active_clusters(n) > 0) {
         pl.nc = n;
         pl.tpc = tpc;
         pl.mode = kCluster;
@@ -786,10 +850,12 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
     const int tpc = (T + cs - 1) / cs;
     if ((T + tpc - 1) / tpc != cs) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;
-    const int act = pl.NM == 1 ? active_clusters<1>(cs) : active_clusters<2>(cs);
+    const int act = active_clusters(cs);
     if (act <= 0) continue;
     const long long waves = (units + act - 1) / act;
-    const long long cost = waves * (tpc + c0 + 1);
+    const long long ctas = units * cs;
+    const long long active = ctas < static_cast<long long>(act) * cs ? ctas : static_cast<long long>(act) * cs;
+    const double cost = makespan(cm, units, pl.rowgroups, tpc, waves, active, cm.cluster_merge);
     if (cost < best) {
       best = cost;
       pl.nc = cs;
@@ -816,30 +882,50 @@ static EncodeFn get_encode() {
   return fn;
 }
 
-static bool encode_kv_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int bs) {
+// Tensor maps of a paged cache [num_blocks, Hkv, bs, 128] bf16, 128-byte swizzle.
+//   kHalfBox: dims {128, bs, Hkv, blocks}, box {64, rows, 1, 1}: one head-dim half of `rows`
+//             rows (rows = min(bs, 64)).
+//   kPageBox: dims {64, bs, 2, Hkv, blocks} (the head dim split into its two halves, the half
+//             index strided by 128 B), box {64, rows, 2, 1, 1}: both halves of `rows` rows in
+//             one copy, landing as [half][rows][64].
+enum MapKind { kHalfBox = 0, kPageBox = 1 };
+
+static bool encode_kv_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int bs, int kind) {
   EncodeFn enc = get_encode();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(bs),
-                              static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(HD) * 2, static_cast<cuuint64_t>(bs) * HD * 2,
-                                 static_cast<cuuint64_t>(Hkv) * bs * HD * 2};
-  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(bs < BN ? bs : BN), 1u, 1u};
-  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint32_t rows = static_cast<cuuint32_t>(bs < 64 ? bs : 64);
+  const cuuint64_t row_b = static_cast<cuuint64_t>(HD) * 2;
+  const cuuint64_t head_b = static_cast<cuuint64_t>(bs) * row_b;
+  const cuuint64_t block_b = static_cast<cuuint64_t>(Hkv) * head_b;
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  if (kind == kHalfBox) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(bs),
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {row_b, head_b, block_b};
+    const cuuint32_t box[4] = {64u, rows, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[5] = {64u, static_cast<cuuint64_t>(bs), 2u, static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {row_b, 128u, head_b, block_b};
+  const cuuint32_t box[5] = {64u, rows, 2u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Small cache of encoded K/V tensor maps keyed by (base pointer, shape): encoding is a
+// Small cache of encoded K/V tensor maps keyed by (base pointer, shape, kind): encoding is a
 // host-side driver call, and serving loops reuse the same cache tensors every step.
 struct MapEntry {
   const void* base;
-  int num_blocks, Hkv, bs;
+  int num_blocks, Hkv, bs, kind;
   CUtensorMap map;
   uint64_t stamp;
 };
 
-static bool cached_kv_map(CUtensorMap* out, const void* base, int num_blocks, int Hkv, int bs) {
+static bool cached_kv_map(CUtensorMap* out, const void* base, int num_blocks, int Hkv, int bs, int kind) {
   constexpr int kSlots = 16;
   static MapEntry cache[kSlots] = {};
   static uint64_t clock = 0;
@@ -849,28 +935,37 @@ static bool cached_kv_map(CUtensorMap* out, const void* base, int num_blocks, in
   int victim = 0;
   for (int i = 0; i < kSlots; ++i) {
     MapEntry& e = cache[i];
-    if (e.stamp != 0 && e.base == base && e.num_blocks == num_blocks && e.Hkv == Hkv && e.bs == bs) {
+    if (e.stamp != 0 && e.base == base && e.num_blocks == num_blocks && e.Hkv == Hkv && e.bs == bs &&
+        e.kind == kind) {
       e.stamp = clock;
       *out = e.map;
       return true;
     }
     if (e.stamp < cache[victim].stamp) victim = i;
   }
-  MapEntry e{base, num_blocks, Hkv, bs, {}, clock};
-  if (!encode_kv_map(&e.map, base, num_blocks, Hkv, bs)) return false;
+  MapEntry e{base, num_blocks, Hkv, bs, kind, {}, clock};
+  if (!encode_kv_map(&e.map, base, num_blocks, Hkv, bs, kind)) return false;
   cache[victim] = e;
   *out = e.map;
   return true;
 }
 
-template <int NM>
-static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, const Plan& pl,
-                     int B, int Hkv, cudaStream_t stream) {
-  if (set_smem_attr<NM>() != cudaSuccess) return TS_ERR_CUDA;
+// A failed CUDA call maps to TS_ERR_CUDA; with TREESPEC_DEBUG set in the environment the
+// call site and the CUDA error string also go to stderr.
+static int cuda_fail(cudaError_t e, const char* where) {
+  if (std::getenv("TREESPEC_DEBUG") != nullptr)
+    std::fprintf(stderr, "treespec: tree_attention %s: %s\n", where, cudaGetErrorString(e));
+  return TS_ERR_CUDA;
+}
+
+static int launch_kernel(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, const Plan& pl, int B,
+                         int Hkv, cudaStream_t stream) {
+  const cudaError_t ea = set_smem_attr();
+  if (ea != cudaSuccess) return cuda_fail(ea, "shared-memory attribute");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.rowgroups, pl.nc, B * Hkv);
-  cfg.blockDim = dim3(Cfg<NM>::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<NM>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -884,7 +979,8 @@ static int launch_nm(const CUtensorMap& mk, const CUtensorMap& mv, const Params&
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<NM>, mk, mv, prm) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, mk, mv, prm);
+  return el == cudaSuccess ? TS_OK : cuda_fail(el, "launch");
 }
 
 }  // namespace tc
@@ -903,7 +999,7 @@ size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefi
 
 void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4) {
   const tc::Plan pl = tc::make_plan(B, m, Hq, Hkv, max_prefix, num_sms);
-  out4[0] = pl.NM;
+  out4[0] = pl.rowgroups;
   out4[1] = pl.nc;
   out4[2] = pl.tpc;
   out4[3] = pl.mode;
@@ -912,9 +1008,9 @@ void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sm
 int attention_tc_launch(const AttnArgs& a, int num_sms) {
   const tc::Plan pl = tc::make_plan(a.B, a.m, a.Hq, a.Hkv, a.max_prefix, num_sms);
   CUtensorMap mk, mv;
-  if (!tc::cached_kv_map(&mk, a.k_cache, a.num_blocks, a.Hkv, a.block_size) ||
-      !tc::cached_kv_map(&mv, a.v_cache, a.num_blocks, a.Hkv, a.block_size))
-    return TS_ERR_CUDA;
+  if (!tc::cached_kv_map(&mk, a.k_cache, a.num_blocks, a.Hkv, a.block_size, tc::kHalfBox) ||
+      !tc::cached_kv_map(&mv, a.v_cache, a.num_blocks, a.Hkv, a.block_size, tc::kPageBox))
+    return tc::cuda_fail(cudaErrorInvalidValue, "tensor map encode");
   tc::Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.block_table = a.block_table;
@@ -942,19 +1038,19 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   prm.part_ml = pl.mode == tc::kGlobal
                     ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * tc::HD * 4)
                     : nullptr;
-  const int rc = pl.NM == 1 ? tc::launch_nm<1>(mk, mv, prm, pl, a.B, a.Hkv, a.stream)
-                            : tc::launch_nm<2>(mk, mv, prm, pl, a.B, a.Hkv, a.stream);
+  const int rc = tc::launch_kernel(mk, mv, prm, pl, a.B, a.Hkv, a.stream);
   if (rc != TS_OK) return rc;
   int launches = 1;
   if (pl.mode == tc::kGlobal) {
     const int total_rows = a.B * a.Hkv * prm.rows;
-    if (launch_pdl(tc::combine_kernel, dim3((total_rows + 7) / 8), dim3(256), 0, a.stream, prm.part_o,
-                   prm.part_ml, a.prefix_len, prm, total_rows) != cudaSuccess)
-      return TS_ERR_CUDA;
+    const cudaError_t ec = launch_pdl(tc::combine_kernel, dim3((total_rows + 7) / 8), dim3(256), 0, a.stream,
+                                      prm.part_o, prm.part_ml, a.prefix_len, prm, total_rows);
+    if (ec != cudaSuccess) return tc::cuda_fail(ec, "combine launch");
     ++launches;
   }
   count_launches(launches);
-  return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+  const cudaError_t eg = cudaGetLastError();
+  return eg == cudaSuccess ? TS_OK : tc::cuda_fail(eg, "after launch");
 }
 
 }  // namespace ts
