@@ -151,11 +151,12 @@ int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, t
                       void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Launch plan ts_tree_attention would use for these sizes on the current device (a
- * diagnostic; the pages have no counterpart).  Writes 5 ints to plan_out: [0] path (0 =
+ * diagnostic; the pages have no counterpart).  Writes 6 ints to plan_out: [0] path (0 =
  * CUDA-core, 1 = tensor-core), [1] row groups of 128 rows (one CTA each), [2] chunks per
- * (sequence, KV head, row group), [3] 128-key tiles per chunk, [4] split mode (0 = one chunk, 1 = chunks
- * merged inside a thread-block cluster, 2 = chunks merged through the workspace).  Returns
- * TS_OK or the validation error ts_tree_attention would return. */
+ * (sequence, KV head, row group), [3] 128-key tiles per chunk, [4] split mode (0 = one chunk,
+ * 1 = chunks merged inside a thread-block cluster, 2 = chunks merged through the workspace),
+ * [5] row groups that share each K/V tile through TMA multicast (1 = none).  Returns TS_OK or
+ * the validation error ts_tree_attention would return. */
 int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
                            int block_size, int* plan_out);
 

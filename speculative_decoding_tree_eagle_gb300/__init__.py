@@ -185,11 +185,11 @@ def tree_attention_plan(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: int, d
                         block_size: int) -> Dict[str, int]:
     """The launch plan tree_attention uses for these sizes on the current device."""
     dt = TS_F32 if dtype == torch.float32 else TS_BF16
-    out = (ctypes.c_int * 5)()
+    out = (ctypes.c_int * 6)()
     _check(library().ts_tree_attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, out))
     modes = {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}
     return {"path": "tensor-core" if out[0] else "cuda-core", "row_groups": out[1], "chunks": out[2],
-            "tiles_per_chunk": out[3], "split": modes.get(out[4], str(out[4]))}
+            "tiles_per_chunk": out[3], "split": modes.get(out[4], str(out[4])), "multicast": out[5]}
 
 
 def tree_accept_workspace(dtype: torch.dtype, B: int, m: int, V: int) -> int:

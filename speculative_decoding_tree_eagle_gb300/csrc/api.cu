@@ -112,6 +112,7 @@ int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, in
     plan_out[2] = 1;
     plan_out[3] = 0;
     plan_out[4] = 0;
+    plan_out[5] = 1;
     return TS_OK;
   }
   plan_out[0] = 1;

@@ -48,8 +48,9 @@ struct AttnArgs {
 bool attention_uses_tc(ts_dtype dt, int d, int block_size);
 size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms);
 int attention_tc_launch(const AttnArgs& a, int num_sms);
-// {row groups of 128 rows, chunks, tiles per chunk, split mode} of the tensor-core launch.
-void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4);
+// {row groups of 128 rows, chunks, tiles per chunk, split mode, multicast width} of the
+// tensor-core launch.
+void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out5);
 int attention_simt_launch(const AttnArgs& a);
 
 // accept_kernel on precomputed per-row partials (value, index) [B*m, S].

@@ -61,7 +61,47 @@ __device__ __forceinline__ void block_best(float& v, int& i) {
   }
 }
 
-// bf16 rows: 8 values per 16-byte load.
+// Running first maximum of one thread over increasing indices: a value replaces the best
+// only when it is strictly larger, so among equal values the first (lowest) index stays and
+// NaN, which compares larger than nothing, is never taken.
+__device__ __forceinline__ void run_max(float& bv, int& bi, float v, int i) {
+  const bool gt = v > bv;
+  bi = gt ? i : bi;
+  bv = gt ? v : bv;
+}
+
+// The 16-byte loads a thread examines: kArgU per batch, kArgThreads apart; the next batch is
+// loaded while the current one is examined (2 x kArgU x 16 B in flight per thread).  Past the
+// segment end the slots hold -inf, which never replaces a best value.  The loads are issued
+// as written (volatile), so the next batch's loads are not moved below the current batch's
+// comparisons.
+constexpr int kArgU = 4;
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// After a thread's scan: if no value above -inf was seen, its answer is its first element
+// that is not NaN (the maximum is -inf there, or nothing but NaN was seen and it stays unset).
+template <typename LoadF>
+__device__ __forceinline__ void first_not_nan(float& bv, int& bi, int begin, int end, int stride, LoadF ld) {
+  if (bi != INT_MAX) return;
+  for (int i = begin; i < end; i += stride) {
+    const float v = ld(i);
+    if (v == v) {
+      bv = v;
+      bi = i;
+      return;
+    }
+  }
+}
+
+// bf16 rows: 8 values per 16-byte load, two independent running maxima (the low and the
+// high four values of every load), merged at the end.
 __global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
     const __nv_bfloat16* __restrict__ logits, int V, int seg_len, int S, int vec,
     float* __restrict__ part_v, int* __restrict__ part_i) {
@@ -70,44 +110,50 @@ __global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
   const long long row = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const __nv_bfloat16* x = logits + row * static_cast<long long>(V);
+  const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
   const int begin = seg * seg_len, end = min(V, begin + seg_len);
   float bv = -INFINITY;
   int bi = INT_MAX;
   if (vec) {
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     const int b8 = begin >> 3, e8 = end >> 3;
-    int i = b8 + threadIdx.x;
-    for (; i + 3 * kArgThreads < e8; i += 4 * kArgThreads) {
-      uint4 a[4];
+    constexpr int step = kArgU * kArgThreads;
+    const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    float bv1 = -INFINITY;
+    int bi1 = INT_MAX;
+    uint4 cur[kArgU], nxt[kArgU];
+    int i0 = b8 + threadIdx.x;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = __ldcs(x8 + i + u * kArgThreads);
+    for (int u = 0; u < kArgU; ++u) cur[u] = i0 + u * kArgThreads < e8 ? ld_stream(x8 + i0 + u * kArgThreads) : ninf;
+    for (; i0 < e8; i0 += step) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int base = (i + u * kArgThreads) << 3;
-        upd(bv, bi, bf16_lo(a[u].x), base + 0);
-        upd(bv, bi, bf16_hi(a[u].x), base + 1);
-        upd(bv, bi, bf16_lo(a[u].y), base + 2);
-        upd(bv, bi, bf16_hi(a[u].y), base + 3);
-        upd(bv, bi, bf16_lo(a[u].z), base + 4);
-        upd(bv, bi, bf16_hi(a[u].z), base + 5);
-        upd(bv, bi, bf16_lo(a[u].w), base + 6);
-        upd(bv, bi, bf16_hi(a[u].w), base + 7);
+      for (int u = 0; u < kArgU; ++u) {
+        const int j = i0 + step + u * kArgThreads;
+        nxt[u] = j < e8 ? ld_stream(x8 + j) : ninf;
       }
+#pragma unroll
+      for (int u = 0; u < kArgU; ++u) {
+        const int base = (i0 + u * kArgThreads) << 3;
+        run_max(bv, bi, bf16_lo(cur[u].x), base + 0);
+        run_max(bv1, bi1, bf16_lo(cur[u].z), base + 4);
+        run_max(bv, bi, bf16_hi(cur[u].x), base + 1);
+        run_max(bv1, bi1, bf16_hi(cur[u].z), base + 5);
+        run_max(bv, bi, bf16_lo(cur[u].y), base + 2);
+        run_max(bv1, bi1, bf16_lo(cur[u].w), base + 6);
+        run_max(bv, bi, bf16_hi(cur[u].y), base + 3);
+        run_max(bv1, bi1, bf16_hi(cur[u].w), base + 7);
+      }
+#pragma unroll
+      for (int u = 0; u < kArgU; ++u) cur[u] = nxt[u];
     }
-    for (; i < e8; i += kArgThreads) {
-      const uint4 a = __ldcs(x8 + i);
-      const int base = i << 3;
-      upd(bv, bi, bf16_lo(a.x), base + 0);
-      upd(bv, bi, bf16_hi(a.x), base + 1);
-      upd(bv, bi, bf16_lo(a.y), base + 2);
-      upd(bv, bi, bf16_hi(a.y), base + 3);
-      upd(bv, bi, bf16_lo(a.z), base + 4);
-      upd(bv, bi, bf16_hi(a.z), base + 5);
-      upd(bv, bi, bf16_lo(a.w), base + 6);
-      upd(bv, bi, bf16_hi(a.w), base + 7);
+    upd(bv, bi, bv1, bi1);
+    // a thread's elements in increasing order: its loads, each load's 8 values
+    if (bi == INT_MAX) {
+      for (int i = b8 + threadIdx.x; i < e8 && bi == INT_MAX; i += kArgThreads)
+        first_not_nan(bv, bi, i << 3, (i << 3) + 8, 1,
+                      [&](int k) { return __uint_as_float(static_cast<uint32_t>(xs[k]) << 16); });
     }
   } else {
-    const unsigned short* xs = reinterpret_cast<const unsigned short*>(x);
     for (int i = begin + threadIdx.x; i < end; i += kArgThreads)
       upd(bv, bi, __uint_as_float(static_cast<uint32_t>(xs[i]) << 16), i);
   }
@@ -118,6 +164,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_bf16_kernel(
   }
 }
 
+// fp32 rows: 4 values per 16-byte load, two running maxima (the first and the second pair).
 __global__ void __launch_bounds__(kArgThreads) argmax_f32_kernel(
     const float* __restrict__ logits, int V, int seg_len, int S, int vec,
     float* __restrict__ part_v, int* __restrict__ part_i) {
@@ -131,13 +178,40 @@ __global__ void __launch_bounds__(kArgThreads) argmax_f32_kernel(
   int bi = INT_MAX;
   if (vec) {
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int i = (begin >> 2) + threadIdx.x; i < (end >> 2); i += kArgThreads) {
-      const float4 a = __ldcs(x4 + i);
-      const int base = i << 2;
-      upd(bv, bi, a.x, base);
-      upd(bv, bi, a.y, base + 1);
-      upd(bv, bi, a.z, base + 2);
-      upd(bv, bi, a.w, base + 3);
+    const int b4 = begin >> 2, e4 = end >> 2;
+    constexpr int step = kArgU * kArgThreads;
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float bv1 = -INFINITY;
+    int bi1 = INT_MAX;
+    float4 cur[kArgU], nxt[kArgU];
+    int i0 = b4 + threadIdx.x;
+    auto ldf4 = [](const float4* q) {
+      const uint4 w = ld_stream(q);
+      return make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
+    };
+#pragma unroll
+    for (int u = 0; u < kArgU; ++u) cur[u] = i0 + u * kArgThreads < e4 ? ldf4(x4 + i0 + u * kArgThreads) : ninf;
+    for (; i0 < e4; i0 += step) {
+#pragma unroll
+      for (int u = 0; u < kArgU; ++u) {
+        const int j = i0 + step + u * kArgThreads;
+        nxt[u] = j < e4 ? ldf4(x4 + j) : ninf;
+      }
+#pragma unroll
+      for (int u = 0; u < kArgU; ++u) {
+        const int base = (i0 + u * kArgThreads) << 2;
+        run_max(bv, bi, cur[u].x, base + 0);
+        run_max(bv1, bi1, cur[u].z, base + 2);
+        run_max(bv, bi, cur[u].y, base + 1);
+        run_max(bv1, bi1, cur[u].w, base + 3);
+      }
+#pragma unroll
+      for (int u = 0; u < kArgU; ++u) cur[u] = nxt[u];
+    }
+    upd(bv, bi, bv1, bi1);
+    if (bi == INT_MAX) {
+      for (int i = b4 + threadIdx.x; i < e4 && bi == INT_MAX; i += kArgThreads)
+        first_not_nan(bv, bi, i << 2, (i << 2) + 4, 1, [&](int k) { return x[k]; });
     }
   } else {
     for (int i = begin + threadIdx.x; i < end; i += kArgThreads) upd(bv, bi, __ldcs(x + i), i);

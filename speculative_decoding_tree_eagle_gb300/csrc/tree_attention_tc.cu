@@ -119,6 +119,7 @@ struct Params {
   float2* part_ml;
   int32_t* status;
   int m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk, mode;
+  int mc;  // row groups sharing each K/V tile through TMA multicast (a cluster along x), 1 = none
   float scale_log2;
 };
 
@@ -191,6 +192,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const int R0 = rg * BM;
   const int rows_here = min(p.rows - R0, BM);
   const int nact = (rows_here + 31) / 32;  // softmax warps that hold rows of this group
+  // Multicast: the mc row groups of one (sequence, KV head, chunk) form a cluster; each CTA
+  // issues 1/mc of every tile's boxes to all of them, so a K/V tile leaves L2 once per
+  // cluster.  A stage may be refilled only when every CTA of the cluster has released it, so
+  // the empty barriers count one release per CTA (the MMA thread's commits are multicast).
+  const int mc = p.mc;
+  const int crank = mc > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << mc) - 1u);
 
   auto bar = [&](int idx) -> uint32_t { return sbase + C::OFF_BAR + 8u * idx; };
   auto full_k = [&](int s) { return bar(s); };
@@ -207,12 +215,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SK; ++s) {
-      mbar_init(full_k(s), C::K_PRODUCERS);  // each producer warp registers its own bytes
-      mbar_init(empty_k(s), 1);
+      mbar_init(full_k(s), C::K_PRODUCERS);  // each producer warp registers its share of the bytes
+      mbar_init(empty_k(s), mc);
     }
     for (int s = 0; s < SV; ++s) {
       mbar_init(full_v(s), C::V_PRODUCERS);
-      mbar_init(empty_v(s), 1);
+      mbar_init(empty_v(s), mc);
     }
     for (int sb = 0; sb < 2; ++sb) {
       mbar_init(s_full(sb), 1);
@@ -314,7 +322,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // V: per box row j one box of both halves (rpb rows x 2 x 128 B, two-half tensor map),
       // placed at j*rpb*256 as [half][rows]: a P V step of 16 keys reads one page.
       const int nbox = kv == 0 ? 2 * bpt : bpt;
-      const int b_begin = part * nbox / nparts, b_end = (part + 1) * nbox / nparts;
+      // boxes this thread issues (its share among the cluster's mc*nparts issuers) and the
+      // bytes it registers on this CTA's barrier (its share of the whole tile, which lands here
+      // whichever CTA issued it)
+      const int gi = crank * nparts + part, ng = mc * nparts;
+      const int b_begin = gi * nbox / ng, b_end = (gi + 1) * nbox / ng;
+      const int x_count = (part + 1) * nbox / nparts - part * nbox / nparts;
       const uint32_t box_bytes = kv == 0 ? rpb * 128 : rpb * 256;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
@@ -323,24 +336,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t fb = kv == 0 ? full_k(s) : full_v(s);
         const uint32_t eb = kv == 0 ? empty_k(s) : empty_v(s);
         if (!mbar_wait(eb, ph ^ 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(fb, static_cast<uint32_t>(b_end - b_begin) * box_bytes);
+        mbar_expect_tx(fb, static_cast<uint32_t>(x_count) * box_bytes);
         if (kv == 0) {
           const uint32_t dst0 = sbase + C::OFF_K + s * KTILE;
           for (int e2 = b_begin; e2 < b_end; ++e2) {
             const int j = e2 >> 1, h = e2 & 1;
             const int blk = s_blk[t * bpt + j];  // num_blocks (out of range) -> zero fill
             const int rin = blk < p.num_blocks ? (j * rpb) & (p.block_size - 1) : 0;
-            tma_load_4d(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk);
+            if (mc > 1)
+              tma_load_4d_mc(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk, mc_mask);
+            else
+              tma_load_4d(dst0 + h * KHALF + j * rpb * 128, map, fb, h * 64, rin, kvh, blk);
           }
         } else {
           const uint32_t dst0 = sbase + C::OFF_V + s * KTILE;
           for (int j = b_begin; j < b_end; ++j) {
             const int blk = s_blk[t * bpt + j];
             const int rin = blk < p.num_blocks ? (j * rpb) & (p.block_size - 1) : 0;
-            tma_load_5d(dst0 + j * rpb * 256, map, fb, 0, rin, 0, kvh, blk);
+            if (mc > 1)
+              tma_load_5d_mc(dst0 + j * rpb * 256, map, fb, 0, rin, 0, kvh, blk, mc_mask);
+            else
+              tma_load_5d(dst0 + j * rpb * 256, map, fb, 0, rin, 0, kvh, blk);
           }
         }
         issued = t + 1;
+      }
+      if (mc > 1 && part == 0 && !*abort_flag) {
+        // every CTA of the cluster has released every stage of this ring: no release of a
+        // peer is still on its way to this CTA's barriers when it exits
+        for (int s = 0; s < ST && s < nt; ++s) {
+          const int uses = (nt - s + ST - 1) / ST;
+          if (!mbar_wait(kv == 0 ? empty_k(s) : empty_v(s), (uses - 1) & 1, abort_flag, p.status)) break;
+        }
       }
       if (*abort_flag) {
         for (int t = max(0, issued - ST); t < issued; ++t)
@@ -388,7 +415,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (!mok) break;
         tc_fence_after();
         qk(t % SK, t & 1);
-        tc_commit(empty_k(t % SK));
+        if (mc > 1) tc_commit_mc(empty_k(t % SK), mc_mask);
+        else tc_commit(empty_k(t % SK));
       }
       for (int t = 0; mok && t < nt; ++t) {
         const int sv = t % SV;
@@ -399,14 +427,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc_fence_after();
         pv(sv, t & 1, t == 0);
         tc_commit(o_ready);
-        tc_commit(empty_v(sv));
+        if (mc > 1) tc_commit_mc(empty_v(sv), mc_mask);
+        else tc_commit(empty_v(sv));
         const int tn = t + 2;
         if (tn < nt) {
           mok = mbar_wait(full_k(tn % SK), (tn / SK) & 1, abort_flag, p.status);
           if (!mok) break;
           tc_fence_after();
           qk(tn % SK, tn & 1);
-          tc_commit(empty_k(tn % SK));
+          if (mc > 1) tc_commit_mc(empty_k(tn % SK), mc_mask);
+          else tc_commit(empty_k(tn % SK));
         }
       }
       tc_commit(o_final);
@@ -490,14 +520,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           l_sum *= alpha;
           m_ref = mt;
         }
-        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // padding rows take an infinite reference, so every exponential of theirs is 0
+        const float mu = !valid ? INFINITY : (m_ref == -INFINITY) ? 0.f : m_ref;
         {
           float rs4[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = valid ? ex2_approx(fmaf(s[2 * c], sl2, -mu)) : 0.f;
-            const float p1 = valid ? ex2_approx(fmaf(s[2 * c + 1], sl2, -mu)) : 0.f;
+            const float x0 = fmaf(s[2 * c], sl2, -mu), x1 = fmaf(s[2 * c + 1], sl2, -mu);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
             rs4[c & 3] += p0 + p1;
             pk[c] = pack_bf16x2(p0, p1);
           }
@@ -667,7 +699,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (mc > 1) cluster_sync_all();  // no CTA leaves while a peer may still address its shared memory
+  else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -739,23 +772,24 @@ static cudaError_t set_smem_attr() {
   return err;
 }
 
-// How many clusters of `cs` CTAs (one per SM) the device runs at once; 0 if unknown.
-static int active_clusters(int cs) {
+// How many clusters of cx x cy CTAs (one per SM) the device runs at once; 0 if unknown.
+static int active_clusters(int cx, int cy) {
   static std::mutex mu;
-  static int cache[kMaxCluster + 1] = {};
-  static bool done[kMaxCluster + 1] = {};
+  static int cache[kMaxCluster + 1][kMaxCluster + 1] = {};
+  static bool done[kMaxCluster + 1][kMaxCluster + 1] = {};
+  if (cx < 1 || cy < 1 || cx * cy > kMaxCluster) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (done[cs]) return cache[cs];
-  done[cs] = true;
+  if (done[cx][cy]) return cache[cx][cy];
+  done[cx][cy] = true;
   if (set_smem_attr() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, cs, 1);
+  cfg.gridDim = dim3(cx, cy, 1);
   cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 1;
-  attr.val.clusterDim.y = cs;
+  attr.val.clusterDim.x = cx;
+  attr.val.clusterDim.y = cy;
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
@@ -764,27 +798,41 @@ static int active_clusters(int cs) {
     cudaGetLastError();
     n = 0;
   }
-  cache[cs] = n;
+  cache[cx][cy] = n;
   return n;
 }
 
 struct Plan {
-  int rowgroups, nc, tpc, mode;
+  int rowgroups, mc, nc, tpc, mode;
 };
+
+// Row groups that share each K/V tile through TMA multicast: all of them up to four, else the
+// largest of 4, 3, 2 that divides their number; 1 when the device cannot co-schedule such
+// clusters or TREESPEC_ATTN_MC=1 is set (tests and tuning).
+static int multicast_width(int rowgroups) {
+  if (const char* ov = std::getenv("TREESPEC_ATTN_MC"))
+    if (std::strcmp(ov, "1") == 0) return 1;
+  int mc = 1;
+  if (rowgroups <= 4) mc = rowgroups;
+  else if (rowgroups % 4 == 0) mc = 4;
+  else if (rowgroups % 3 == 0) mc = 3;
+  else if (rowgroups % 2 == 0) mc = 2;
+  if (mc > 1 && active_clusters(mc, 1) <= 0) mc = 1;
+  return mc;
+}
 
 // Makespan model (microseconds).  A CTA streams tpc tiles of 128 keys at the larger of its
 // own pipeline rate (tau_c per tile) and its share of the HBM bandwidth when `active` CTAs
-// stream at once (each K/V tile is 64 KB; row groups past the first read it from L2), plus a
-// fixed cost per CTA (set-up, pipeline fill and drain, epilogue) and the merge of the split.
+// stream at once (each K/V tile is 64 KB, shared by the row groups of a unit), plus a fixed
+// cost per CTA (set-up, pipeline fill and drain, epilogue) and the merge of the split.
 struct CostModel {
   double tau_c, c0, hbm_bytes_per_us, cluster_merge, global_merge;
 };
 
-static double makespan(const CostModel& cm, long long units, int unit_groups, int tpc, long long waves,
-                       long long active, double merge) {
+static double makespan(const CostModel& cm, int unit_groups, int tpc, long long waves, long long active,
+                       double merge) {
   const double tau_h = 65536.0 * static_cast<double>(active) / static_cast<double>(unit_groups) / cm.hbm_bytes_per_us;
   const double tau = cm.tau_c > tau_h ? cm.tau_c : tau_h;
-  (void)units;
   return static_cast<double>(waves) * (tpc * tau + cm.c0) + merge;
 }
 
@@ -795,7 +843,13 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
   pl.rowgroups = (rows + BM - 1) / BM;
   const int T = (max_prefix + m + BN - 1) / BN;
   const long long units = static_cast<long long>(B) * Hkv * pl.rowgroups;
-  const CostModel cm{0.75, 2.5, 6.5e6, 1.5, 3.0};
+  pl.mc = multicast_width(pl.rowgroups);
+  // CTAs resident at once: clusters of mc row groups are placed whole
+  long long slots = num_sms;
+  if (pl.mc > 1) slots = static_cast<long long>(active_clusters(pl.mc, 1)) * pl.mc;
+  // calibrated on the GB300 (128-row CTAs: ~1.25 us per 128-key tile; ~20 us per CTA of set-up,
+  // pipeline fill, drain and epilogue, which makes fewer and longer CTAs the better split)
+  const CostModel cm{1.25, 20.0, 6.5e6, 1.5, 3.0};
   double best = -1.0;
   pl.nc = 1;
   pl.tpc = T;
@@ -806,9 +860,9 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
     if ((T + tpc - 1) / tpc != nc) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;  // box ids staged for the smallest pages
     const long long ctas = units * nc;
-    const long long waves = (ctas + num_sms - 1) / num_sms;
-    const long long active = ctas < num_sms ? ctas : num_sms;
-    const double cost = makespan(cm, units, pl.rowgroups, tpc, waves, active, nc > 1 ? cm.global_merge : 0.0);
+    const long long waves = (ctas + slots - 1) / slots;
+    const long long active = ctas < slots ? ctas : slots;
+    const double cost = makespan(cm, pl.rowgroups, tpc, waves, active, nc > 1 ? cm.global_merge : 0.0);
     if (best < 0 || cost < best) {
       best = cost;
       pl.nc = nc;
@@ -817,7 +871,8 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
     }
   }
   // Optional override for tests and tuning: TREESPEC_ATTN_SPLIT=direct | cluster:N | global:N
-  // (ignored when the requested split is not feasible for these sizes).
+  // (ignored when the requested split is not feasible for these sizes; the chunk cluster is
+  // only used without multicast).
   if (const char* ov = std::getenv("TREESPEC_ATTN_SPLIT")) {
     int n = 0;
     if (std::strcmp(ov, "direct") == 0) {
@@ -827,9 +882,9 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
         pl.mode = kDirect;
         return pl;
       }
-    } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n) {
+    } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n && pl.mc == 1) {
       const int tpc = (T + n - 1) / n;
-      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && active_clusters(n) > 0) {
+      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && active_clusters(1, n) > 0) {
         pl.nc = n;
         pl.tpc = tpc;
         pl.mode = kCluster;
@@ -845,17 +900,18 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
       }
     }
   }
+  if (pl.mc > 1) return pl;
   for (int cs = 2; cs <= kMaxCluster; cs *= 2) {
     if (T < cs) break;
     const int tpc = (T + cs - 1) / cs;
     if ((T + tpc - 1) / tpc != cs) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;
-    const int act = active_clusters(cs);
+    const int act = active_clusters(1, cs);
     if (act <= 0) continue;
     const long long waves = (units + act - 1) / act;
     const long long ctas = units * cs;
     const long long active = ctas < static_cast<long long>(act) * cs ? ctas : static_cast<long long>(act) * cs;
-    const double cost = makespan(cm, units, pl.rowgroups, tpc, waves, active, cm.cluster_merge);
+    const double cost = makespan(cm, pl.rowgroups, tpc, waves, active, cm.cluster_merge);
     if (cost < best) {
       best = cost;
       pl.nc = cs;
@@ -972,10 +1028,10 @@ static int launch_kernel(const CUtensorMap& mk, const CUtensorMap& mv, const Par
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (pl.mode == kCluster) {
+  if (pl.mode == kCluster || pl.mc > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = pl.nc;
+    attr[1].val.clusterDim.x = pl.mc;
+    attr[1].val.clusterDim.y = pl.mode == kCluster ? pl.nc : 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
@@ -997,12 +1053,13 @@ size_t attention_tc_workspace_bytes(int B, int m, int Hq, int Hkv, int max_prefi
   return prow * tc::HD * 4 + prow * 8 + 512;
 }
 
-void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out4) {
+void attention_tc_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms, int* out5) {
   const tc::Plan pl = tc::make_plan(B, m, Hq, Hkv, max_prefix, num_sms);
-  out4[0] = pl.rowgroups;
-  out4[1] = pl.nc;
-  out4[2] = pl.tpc;
-  out4[3] = pl.mode;
+  out5[0] = pl.rowgroups;
+  out5[1] = pl.nc;
+  out5[2] = pl.tpc;
+  out5[3] = pl.mode;
+  out5[4] = pl.mc;
 }
 
 int attention_tc_launch(const AttnArgs& a, int num_sms) {
@@ -1032,6 +1089,7 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   prm.tpc = pl.tpc;
   prm.nchunk = pl.nc;
   prm.mode = pl.mode;
+  prm.mc = pl.mc;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   const size_t prow = static_cast<size_t>(a.B) * a.Hkv * prm.rows * pl.nc;
   prm.part_o = pl.mode == tc::kGlobal ? static_cast<float*>(a.workspace) : nullptr;

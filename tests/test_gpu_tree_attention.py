@@ -53,8 +53,8 @@ def _small(name, **kw):
     return w, inp, tree
 
 
-# (B, Hq, Hkv, d, prefix range, m, k, depth): rows = m*Hq/Hkv spans 1 or 2 M tiles; the
-# prefixes span several 64-key tiles and end mid-tile; some force split-K over chunks.
+# (B, Hq, Hkv, d, prefix range, m, k, depth): rows = m*Hq/Hkv spans 1 to 4 row groups of 128
+# rows; the prefixes span several 128-key tiles and end mid-tile; some force split-K over chunks.
 SMALL = [
     dict(B=2, Hq=8, Hkv=2, prefix=(150, 150), m=8, k=2, depth=3),            # 32 rows, one M tile
     dict(B=3, Hq=8, Hkv=2, prefix=(1, 700), m=8, k=2, depth=3),              # ragged prefixes
@@ -141,21 +141,31 @@ def test_workloads_full_size_sampled(name):
 
 
 SPLITS = [("direct", 0), ("cluster:2", 1), ("cluster:4", 1), ("cluster:8", 1), ("global:3", 2), ("global:11", 2)]
-ROW_CASES = [dict(B=2, Hq=8, Hkv=2, m=30, k=5, depth=6),      # 120 rows: one M tile, double-buffered S
-             dict(B=1, Hq=16, Hkv=4, m=60, k=8, depth=6)]     # 240 rows: two M tiles
+ROW_CASES = [dict(B=2, Hq=8, Hkv=2, m=30, k=5, depth=6),      # 120 rows: one row group
+             dict(B=1, Hq=16, Hkv=4, m=60, k=8, depth=6)]     # 240 rows: two row groups
 
 
-@pytest.mark.parametrize("rows_case", ROW_CASES, ids=["one_m_tile", "two_m_tiles"])
+@pytest.mark.parametrize("multicast", [True, False], ids=["multicast", "no_multicast"])
+@pytest.mark.parametrize("rows_case", ROW_CASES, ids=["one_row_group", "two_row_groups"])
 @pytest.mark.parametrize("split,mode", SPLITS, ids=[s for s, _ in SPLITS])
-def test_every_split_mode_repeated_calls(split, mode, rows_case, monkeypatch):
+def test_every_split_mode_repeated_calls(split, mode, rows_case, multicast, monkeypatch):
     """Force each way of splitting a sequence over CTAs (one chunk, chunks merged inside a
     cluster, chunks merged through the workspace) with chunks long enough to wrap the K/V
-    ring several times; five calls in a row must agree exactly and match the oracle."""
+    ring several times, with and without the row groups sharing K/V tiles by multicast;
+    five calls in a row must agree exactly and match the oracle."""
     lib()
+    rows = rows_case["m"] * rows_case["Hq"] // rows_case["Hkv"]
+    if rows <= 128 and not multicast:
+        pytest.skip("one row group: nothing to multicast")
+    if rows > 128 and multicast and split.startswith("cluster"):
+        pytest.skip("the chunk cluster is used without multicast only")
     monkeypatch.setenv("TREESPEC_ATTN_SPLIT", split)
+    if not multicast:
+        monkeypatch.setenv("TREESPEC_ATTN_MC", "1")
     w, inp, tree = _small("attn_split", prefix=(1900, 1900), **rows_case)
     plan = ts.tree_attention_plan(inp["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix, 16)
     assert plan["split"] == {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}[mode], plan
+    assert plan["multicast"] == (2 if rows > 128 and multicast else 1), plan
     g = {k: inp[k].to(dev()) for k in ("q", "k_cache", "v_cache", "block_table", "prefix_len")}
     first = None
     for _ in range(5):
@@ -170,3 +180,41 @@ def test_every_split_mode_repeated_calls(split, mode, rows_case, monkeypatch):
     ref, _ = oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
                                    inp["prefix_len"].numpy(), tree["mask"], scale_of(w))
     assert_attention_close(first, ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("cfg", [dict(B=3, Hq=32, Hkv=8, prefix=(100, 2000), m=64, k=10, depth=7),    # 2 row groups
+                                 dict(B=2, Hq=64, Hkv=8, prefix=(700, 1500), m=60, k=8, depth=6),     # 4 row groups
+                                 dict(B=2, Hq=24, Hkv=2, prefix=(300, 900), m=32, k=6, depth=5)],     # 3 row groups
+                         ids=["2_groups", "4_groups", "3_groups"])
+def test_multicast_equals_separate_loads(cfg, monkeypatch):
+    """Row groups that receive their K/V tiles by TMA multicast compute exactly what they
+    compute from their own loads (ragged prefixes, garbage past each sequence's end); the
+    split is fixed (one chunk) so that the two runs sum in the same order."""
+    lib()
+    monkeypatch.setenv("TREESPEC_ATTN_SPLIT", "direct")
+    w, inp, tree = _small("attn_mc", **cfg)
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    bs = kc.shape[2]
+    for b in range(w.B):
+        n = int(inp["prefix_len"][b]) + w.m
+        last = int(inp["block_table"][b, (n - 1) // bs])
+        if n % bs:
+            kc[last, :, n % bs:, :] = float("nan")
+            vc[last, :, n % bs:, :] = float("inf")
+    inp = dict(inp, k_cache=kc, v_cache=vc)
+    g = {k: inp[k].to(dev()) for k in ("q", "k_cache", "v_cache", "block_table", "prefix_len")}
+    outs = []
+    for mc in ("default", "1"):
+        if mc == "1":
+            monkeypatch.setenv("TREESPEC_ATTN_MC", "1")
+        plan = ts.tree_attention_plan(inp["q"].dtype, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix, 16)
+        assert (plan["multicast"] > 1) == (mc == "default"), plan
+        status = ts.new_status(dev())
+        out, lse = ts.tree_attention(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["prefix_len"],
+                                     words_i64(tree["mask_words"]), max_prefix=w.max_prefix, status=status)
+        ts.check_status(status)
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ref, _ = oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
+                                   inp["prefix_len"].numpy(), tree["mask"], scale_of(w))
+    assert_attention_close(outs[0][0], ref, torch.bfloat16)
