@@ -169,7 +169,9 @@ int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, in
  * logits     [B, m, V] (dt), row (b, i) = target distribution after node i's root path.
  * tokens, parents [B, m] int32 (as from ts_tree_build; parents precede children).
  * Outputs:
- *   argmax      [B, m] int32, first index of the row maximum (ties -> lowest id).
+ *   argmax      [B, m] int32, first index of the row maximum (ties -> lowest id; -0 == +0).
+ *               NaN entries are never the argmax (-inf is an ordinary value); a row of
+ *               nothing but NaN gives -1, which matches no token.
  *   accept_len  [B] int32 >= 1: nodes on the accepted path, root included.
  *   accept_path [B, m] int32: flat indices root..accepted node, then -1.
  *   bonus       [B] int32: argmax at the accepted node (the token the step emits after

@@ -30,7 +30,7 @@ Parity status of each function is stated in its module header.
 """
 from .tree_build import row_topk, tree_build, ancestor_mask, mask_to_words, words_to_mask  # noqa: F401
 from .tree_attention import tree_attention  # noqa: F401
-from .tree_accept import target_argmax, accept_longest_path  # noqa: F401
+from .tree_accept import target_argmax, target_argmax_ignoring_nan, accept_longest_path  # noqa: F401
 from .kv_commit import kv_commit  # noqa: F401
 from .lm_head import lm_head_logits, lm_head_argmax, fp32_error_bound  # noqa: F401
 from .efficient_head import candidates, efficient_head  # noqa: F401

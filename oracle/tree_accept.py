@@ -14,6 +14,9 @@ Definitions:
 * ``target_argmax``: per (b, node) the vocabulary index of the largest logit; equal
   values -> lowest index (numpy's argmax returns the first maximum).  Values are compared
   exactly as given (bf16 logits are widened without rounding).
+* ``target_argmax_ignoring_nan``: the same over the values that are not NaN (the pages'
+  logits are finite; this fixes what a NaN row entry does: it is never the argmax, -inf
+  counts as a value, and a row with nothing but NaN gives -1).
 * ``accept_longest_path``: a node is *valid* if every non-root node on its root path
   carries the token equal to the target argmax at its parent.  The accepted node is the
   valid node of greatest depth (ties -> lowest flat index).  ``accept_len`` = its depth
@@ -35,6 +38,26 @@ def target_argmax(logits) -> np.ndarray:
         import torch
         logits = logits.detach().to(torch.float32).cpu().numpy()
     return np.argmax(np.asarray(logits), axis=-1).astype(np.int64)
+
+
+def target_argmax_ignoring_nan(logits) -> np.ndarray:
+    """[B, m, V] -> int64 [B, m]: first index of the largest value that is not NaN; -1 for a
+    row of NaN only.  Written as an explicit loop over the rows."""
+    if hasattr(logits, "detach"):
+        import torch
+        logits = logits.detach().to(torch.float32).cpu().numpy()
+    x = np.asarray(logits)
+    B, m, V = x.shape
+    out = np.full((B, m), -1, dtype=np.int64)
+    for b in range(B):
+        for i in range(m):
+            row = x[b, i]
+            keep = np.nonzero(~np.isnan(row))[0]
+            if len(keep) == 0:
+                continue
+            best = row[keep].max()
+            out[b, i] = int(keep[row[keep] == best][0])
+    return out
 
 
 def accept_one(tokens, parents, amax):

@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(
     int bi = INT_MAX;
 #pragma unroll 4
     for (int s = 0; s < S; ++s) upd(bv, bi, part_v[(r0 + i) * S + s], part_i[(r0 + i) * S + s]);
+    if (bi == INT_MAX) bi = -1;  // nothing but NaN in the row
     s_amax[i] = bi;
     argmax[r0 + i] = bi;
     const int p = parents[r0 + i];

@@ -117,3 +117,36 @@ def test_bad_parents_reported():
     assert int(status.item()) == -6
     assert got["accept_len"].tolist()[1] == 0 and got["bonus"].tolist()[1] == -1
     assert got["accept_path"][1].tolist() == [-1, -1, -1, -1]
+
+
+@pytest.mark.parametrize("V,dtype", [(1000, torch.bfloat16), (4099, torch.float32), (128256, torch.bfloat16)])
+def test_nan_logits_are_never_the_argmax(V, dtype):
+    """Rows with NaN entries (before, at and after the maximum, a row of NaN only, NaN beside
+    -inf only): the argmax is the first largest non-NaN entry, -1 for a row of NaN only."""
+    lib()
+    g = torch.Generator().manual_seed(V + 3)
+    B, m = 2, 9
+    logits = torch.round(torch.randn(B, m, V, generator=g) * 2)
+    nan, inf = float("nan"), float("inf")
+    logits[0, 0, : V // 2] = nan                 # NaN before the maximum
+    mx = int(logits[0, 1].argmax())
+    logits[0, 1, mx] = nan                       # NaN where the maximum was
+    logits[0, 2, -5:] = nan                      # NaN at the end
+    logits[0, 3] = nan                           # nothing but NaN
+    logits[0, 4] = -inf
+    logits[0, 4, ::3] = nan                      # -inf and NaN only
+    logits[1, ::2, 7] = nan
+    logits = logits.to(dtype)
+    parents = np.tile(np.array([-1, 0, 0, 1, 1, 2, 3, 5, 7]), (B, 1))
+    tokens = np.tile(np.arange(9), (B, 1))
+    status = ts.new_status(dev())
+    got = ts.tree_accept(logits.to(dev()), torch.as_tensor(tokens, dtype=torch.int32, device=dev()),
+                         torch.as_tensor(parents, dtype=torch.int32, device=dev()), status=status)
+    ts.check_status(status)
+    amax = oracle.target_argmax_ignoring_nan(logits)
+    assert amax[0, 3] == -1
+    np.testing.assert_array_equal(got["argmax"].cpu().numpy(), amax)
+    lens, paths, bonus = oracle.accept_longest_path(tokens, parents, amax)
+    np.testing.assert_array_equal(got["accept_len"].cpu().numpy(), lens)
+    np.testing.assert_array_equal(got["accept_path"].cpu().numpy(), paths)
+    np.testing.assert_array_equal(got["bonus"].cpu().numpy(), bonus)

@@ -92,3 +92,30 @@ def test_batched_shapes():
     lens, paths, bonus = accept_longest_path(np.array([[1, 2], [3, 4]]), np.array([[-1, 0], [-1, 0]]),
                                              np.array([[2, 0], [0, 0]]))
     assert lens.tolist() == [2, 1] and paths.tolist() == [[0, 1], [0, -1]] and bonus.tolist() == [0, 0]
+
+
+def test_argmax_ignoring_nan_hand_cases():
+    """NaN is never the argmax, -inf is an ordinary value, a row of NaN only gives -1."""
+    from oracle import target_argmax_ignoring_nan
+    nan, inf = float("nan"), float("inf")
+    rows = [[nan, 1.0, 3.0, 3.0], [nan, -inf, -inf, nan], [nan, nan, nan, nan], [3.0, nan, 3.0, 2.0],
+            [-inf, nan, 5.0, nan], [-0.0, 0.0, nan, -1.0]]
+    got = target_argmax_ignoring_nan(np.array([rows]))
+    assert got.tolist() == [[2, 1, -1, 0, 2, 0]]
+
+
+def test_argmax_ignoring_nan_equals_a_sort_over_the_kept_entries():
+    """Random rows with NaNs sprinkled: the answer is the first entry of the kept (value,
+    index) pairs sorted by value descending, index ascending; without NaN it is np.argmax."""
+    from oracle import target_argmax_ignoring_nan
+    rng = np.random.default_rng(5)
+    x = np.round(rng.normal(size=(3, 40, 23)) * 2)
+    x[rng.random(x.shape) < 0.3] = np.nan
+    x[0, 0] = np.nan
+    got = target_argmax_ignoring_nan(x)
+    for b in range(3):
+        for i in range(40):
+            kept = sorted((-v, j) for j, v in enumerate(x[b, i]) if not np.isnan(v))
+            assert got[b, i] == (kept[0][1] if kept else -1)
+    clean = np.round(rng.normal(size=(2, 7, 50)))
+    assert np.array_equal(target_argmax_ignoring_nan(clean), target_argmax(clean))
