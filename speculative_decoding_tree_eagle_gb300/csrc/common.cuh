@@ -87,37 +87,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-#ifdef TS_SPIN_WAIT
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
-      : "memory");
-#endif
-  return ok != 0;
-}
-
-// As mbar_try, but a thread whose phase is not complete yet may be suspended for up to
-// `ns` nanoseconds (it resumes as soon as the phase completes), so that waiting warps leave
-// the issue slots of their scheduler to the warps that compute.
-__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
@@ -133,11 +108,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-#ifdef TS_WAIT_SUSPEND_NS
-    if (mbar_try_suspend(bar, parity, TS_WAIT_SUSPEND_NS)) return true;
-#else
     if (mbar_try(bar, parity)) return true;
-#endif
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -206,13 +177,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, uint
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
-}
-
-// Asynchronous prefetch of `bytes` contiguous global bytes into L2 (address 16-byte aligned,
-// size a multiple of 16); no completion is tracked.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
