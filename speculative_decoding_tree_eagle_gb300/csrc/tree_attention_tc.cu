@@ -196,9 +196,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // issues 1/mc of every tile's boxes to all of them, so a K/V tile leaves L2 once per
   // cluster.  A stage may be refilled only when every CTA of the cluster has released it, so
   // the empty barriers count one release per CTA (the MMA thread's commits are multicast).
+  // The cluster is mc x nc CTAs in the chunk-merge mode (rank = x + mc*y), mc x 1 otherwise;
+  // the row groups of one chunk (same y) share the multicasts.
   const int mc = p.mc;
-  const int crank = mc > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const uint16_t mc_mask = static_cast<uint16_t>((1u << mc) - 1u);
+  const int crank = rg % mc;
+  const uint16_t mc_mask =
+      static_cast<uint16_t>(((1u << mc) - 1u) << (p.mode == kCluster ? mc * chunk : 0));
 
   auto bar = [&](int idx) -> uint32_t { return sbase + C::OFF_BAR + 8u * idx; };
   auto full_k = [&](int s) { return bar(s); };
@@ -630,7 +633,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     //    stores (no round trips); 3) barrier: all pushes are visible; 4) each owner merges
     //    its rows from local shared memory and writes the output.
     const int cs = p.nchunk;
-    const int q = static_cast<int>(cluster_ctarank());
+    const int q = chunk;  // this CTA's place among the chunks of its row group
+    auto rank_of = [&](int c) { return static_cast<uint32_t>(crank + mc * c); };
     const int per = BM / cs;  // cs divides 128
     tc_fence_before();
     cluster_sync_all();
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int slot = q * per + (Rl - owner * per);
       if (hh == 0) {
         const float2 ml = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
-        st_dsmem_f2(dsmem_addr(sbase + C::OFF_ML + 8u * slot, owner), ml);
+        st_dsmem_f2(dsmem_addr(sbase + C::OFF_ML + 8u * slot, rank_of(owner)), ml);
       }
       if (__any_sync(0xffffffffu, have)) {  // tcgen05.ld is warp-wide
         tc_fence_after();
@@ -654,7 +658,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (have) {
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              st_dsmem_u4(dsmem_addr(sbase + C::OFF_K + orow_off(slot, 16 * hh + cc * 8 + v4), owner),
+              st_dsmem_u4(dsmem_addr(sbase + C::OFF_K + orow_off(slot, 16 * hh + cc * 8 + v4), rank_of(owner)),
                           make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]));
           }
         }
@@ -882,9 +886,10 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
         pl.mode = kDirect;
         return pl;
       }
-    } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n && pl.mc == 1) {
+    } else if (std::sscanf(ov, "cluster:%d", &n) == 1 && (n == 2 || n == 4 || n == 8) && T >= n &&
+               pl.mc * n <= kMaxCluster) {
       const int tpc = (T + n - 1) / n;
-      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && active_clusters(1, n) > 0) {
+      if ((T + tpc - 1) / tpc == n && tpc * (BN / 16) <= kMaxChunkBoxes && active_clusters(pl.mc, n) > 0) {
         pl.nc = n;
         pl.tpc = tpc;
         pl.mode = kCluster;
@@ -900,17 +905,18 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
       }
     }
   }
-  if (pl.mc > 1) return pl;
-  for (int cs = 2; cs <= kMaxCluster; cs *= 2) {
+  for (int cs = 2; pl.mc * cs <= kMaxCluster; cs *= 2) {
     if (T < cs) break;
     const int tpc = (T + cs - 1) / cs;
     if ((T + tpc - 1) / tpc != cs) continue;
     if (tpc * (BN / 16) > kMaxChunkBoxes) continue;
-    const int act = active_clusters(1, cs);
+    const int act = active_clusters(pl.mc, cs);  // clusters of mc row groups x cs chunks
     if (act <= 0) continue;
-    const long long waves = (units + act - 1) / act;
+    const long long clusters = units / pl.mc;
+    const long long waves = (clusters + act - 1) / act;
     const long long ctas = units * cs;
-    const long long active = ctas < static_cast<long long>(act) * cs ? ctas : static_cast<long long>(act) * cs;
+    const long long active = ctas < static_cast<long long>(act) * pl.mc * cs ? ctas
+                                                                            : static_cast<long long>(act) * pl.mc * cs;
     const double cost = makespan(cm, pl.rowgroups, tpc, waves, active, cm.cluster_merge);
     if (cost < best) {
       best = cost;

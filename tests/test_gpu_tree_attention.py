@@ -157,8 +157,8 @@ def test_every_split_mode_repeated_calls(split, mode, rows_case, multicast, monk
     rows = rows_case["m"] * rows_case["Hq"] // rows_case["Hkv"]
     if rows <= 128 and not multicast:
         pytest.skip("one row group: nothing to multicast")
-    if rows > 128 and multicast and split.startswith("cluster"):
-        pytest.skip("the chunk cluster is used without multicast only")
+    if rows > 128 and multicast and split == "cluster:8":
+        pytest.skip("2 row groups x 8 chunks exceed the largest cluster (8 CTAs)")
     monkeypatch.setenv("TREESPEC_ATTN_SPLIT", split)
     if not multicast:
         monkeypatch.setenv("TREESPEC_ATTN_MC", "1")
