@@ -69,6 +69,7 @@ constexpr uint32_t KTILE = 2 * KHALF;  // 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxChunkBoxes = 2048;       // physical-block ids a CTA stages in shared memory
 constexpr int kMaxCluster = 8;
+constexpr int kMaxSortedSeqs = 64;  // batches up to this size are dispatched longest first
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum Mode { kDirect = 0, kCluster = 1, kGlobal = 2 };
@@ -118,7 +119,7 @@ struct Params {
   float* part_o;
   float2* part_ml;
   int32_t* status;
-  int m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk, mode;
+  int B, m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk, mode;
   int mc;  // row groups sharing each K/V tile through TMA multicast (a cluster along x), 1 = none
   float scale_log2;
 };
@@ -170,9 +171,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   unsigned char* sptr = smem_raw + (sbase - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = blockIdx.x, chunk = blockIdx.y, bk = blockIdx.z;
-  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const int rg = blockIdx.x, chunk = blockIdx.y;
+  const int slot = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
   pdl_wait();
+  // Launch order by decreasing prefix length (ties -> lower index): the CTAs of the longest
+  // sequences are dispatched first and the short ones fill in behind them.
+  int b = slot;
+  if (p.B > 1 && p.B <= kMaxSortedSeqs) {
+    int* s_len = reinterpret_cast<int*>(sptr + C::OFF_BLK);  // (the block-id area, not used yet)
+    int* s_pick = s_len + kMaxSortedSeqs;
+    if (threadIdx.x < p.B) s_len[threadIdx.x] = p.prefix_len[threadIdx.x];
+    __syncthreads();
+    if (threadIdx.x < p.B) {
+      const int Lb = s_len[threadIdx.x];
+      int rank = 0;
+      for (int j = 0; j < p.B; ++j) {
+        const int Lj = s_len[j];
+        rank += (Lj > Lb) | ((Lj == Lb) & (j < static_cast<int>(threadIdx.x)));
+      }
+      if (rank == slot) *s_pick = threadIdx.x;
+    }
+    __syncthreads();
+    b = *s_pick;
+    __syncthreads();
+  }
+  const int bk = b * p.Hkv + kvh;
   const int L = p.prefix_len[b];
   // (the whole cluster shares b, so every CTA of a cluster returns here together)
   if (L < 0 || L > p.max_prefix) {
@@ -181,14 +204,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   }
   const int nkeys = L + p.m;
   const int T = (nkeys + BN - 1) / BN;
-  // balanced chunks: chunk c covers tiles [ceil(c*T/nc), ceil((c+1)*T/nc)) of this sequence,
-  // so the chunks that get one tile more are the first ones and the last chunk, which holds
-  // the masked tree tile, is never the longest
-  const int t0 = static_cast<int>((static_cast<long long>(chunk) * T + p.nchunk - 1) / p.nchunk);
-  const int nt = static_cast<int>((static_cast<long long>(chunk + 1) * T + p.nchunk - 1) / p.nchunk) - t0;
+  // chunk c covers tiles [c*tpc, (c+1)*tpc) of this sequence (tpc from the longest allowed
+  // prefix), so a shorter sequence uses fewer chunks and its CTAs past the end leave at once;
+  // the last chunk, which holds the masked tree tile, is never the longest
+  const int t0 = chunk * p.tpc;
+  const int nt = max(0, min(T, t0 + p.tpc) - t0);
   if (nt == 0 && p.mode != kCluster) return;  // (an idle CTA of a cluster still merges)
   // a sequence whose tiles all fall into one chunk is written directly also in the global mode
-  const bool direct = p.mode == kDirect || (p.mode == kGlobal && min(T, p.nchunk) == 1);
+  const bool direct = p.mode == kDirect || (p.mode == kGlobal && T <= p.tpc);
   const int R0 = rg * BM;
   const int rows_here = min(p.rows - R0, BM);
   const int nact = (rows_here + 31) / 32;  // softmax warps that hold rows of this group
@@ -728,12 +751,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (L < 0 || L > p.max_prefix) return;
   const int T = (L + p.m + BN - 1) / BN;
   const int nc = p.nchunk;
-  if (min(T, nc) <= 1) return;  // written directly by the attention kernel
+  if (T <= p.tpc) return;  // one chunk: written directly by the attention kernel
   const long long prow = static_cast<long long>(wid) * nc;
-  // chunk c holds tiles [ceil(c*T/nc), ceil((c+1)*T/nc)); empty chunks wrote nothing
-  auto empty = [&](int c) {
-    return (static_cast<long long>(c + 1) * T + nc - 1) / nc == (static_cast<long long>(c) * T + nc - 1) / nc;
-  };
+  // chunk c holds tiles [c*tpc, (c+1)*tpc); chunks past the end wrote nothing
+  auto empty = [&](int c) { return c * p.tpc >= T; };
   float M = -INFINITY;
 #pragma unroll 4
   for (int c = 0; c < nc; ++c) {
@@ -872,6 +893,19 @@ static Plan make_plan(int B, int m, int Hq, int Hkv, int max_prefix, int num_sms
       pl.nc = nc;
       pl.tpc = tpc;
       pl.mode = nc > 1 ? kGlobal : kDirect;
+    }
+  }
+  // The model assumes every sequence is max_prefix long.  When it keeps one chunk and a wave
+  // of such CTAs leaves SMs idle, a batch of several sequences is split in two chunks of
+  // ceil(T/2) tiles: with prefixes of mixed lengths only the sequences longer than that use the
+  // second chunk (the others' CTAs leave at once), and the longest sequences, dispatched
+  // first, no longer set the whole call's length.
+  if (pl.nc == 1 && B > 1 && units < num_sms && T >= 4) {
+    const int tpc = (T + 1) / 2;
+    if (tpc * (BN / 16) <= kMaxChunkBoxes) {
+      pl.nc = 2;
+      pl.tpc = tpc;
+      pl.mode = kGlobal;
     }
   }
   // Optional override for tests and tuning: TREESPEC_ATTN_SPLIT=direct | cluster:N | global:N
@@ -1082,6 +1116,7 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.lse = a.lse;
   prm.status = a.dev_status;
+  prm.B = a.B;
   prm.m = a.m;
   prm.Hq = a.Hq;
   prm.Hkv = a.Hkv;

@@ -218,3 +218,17 @@ def test_multicast_equals_separate_loads(cfg, monkeypatch):
     ref, _ = oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
                                    inp["prefix_len"].numpy(), tree["mask"], scale_of(w))
     assert_attention_close(outs[0][0], ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("split", ["auto", "global:2", "global:3", "direct"])
+def test_ragged_batch_longest_first(split, monkeypatch):
+    """Sequences of very different lengths (several shorter than one chunk): the CTAs are
+    dispatched longest sequence first and short sequences leave their later chunks empty;
+    every output matches the oracle."""
+    lib()
+    if split != "auto":
+        monkeypatch.setenv("TREESPEC_ATTN_SPLIT", split)
+    w, inp, tree = _small("attn_ragged", B=6, Hq=16, Hkv=4, prefix=(5, 3000), m=16, k=4, depth=4)
+    lens = inp["prefix_len"].tolist()
+    assert max(lens) - min(lens) > 1000, lens
+    _run(inp, w, tree["mask"], tree["mask_words"])
