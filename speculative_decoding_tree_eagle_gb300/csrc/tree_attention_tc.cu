@@ -753,29 +753,40 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int nc = p.nchunk;
   if (T <= p.tpc) return;  // one chunk: written directly by the attention kernel
   const long long prow = static_cast<long long>(wid) * nc;
-  // chunk c holds tiles [c*tpc, (c+1)*tpc); chunks past the end wrote nothing
-  auto empty = [&](int c) { return c * p.tpc >= T; };
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int c = 0; c < nc; ++c) {
-    if (empty(c)) continue;
-    const float2 ml = part_ml[prow + c];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
+  // chunk c holds tiles [c*tpc, (c+1)*tpc); chunks past the end wrote nothing.  The used
+  // chunks are merged four at a time, all their loads issued before any is used, into a
+  // running (max, sum, O) in the log2 domain.
+  const int used = min(nc, (T + p.tpc - 1) / p.tpc);
+  float M = -INFINITY, Ls = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Ls = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < nc; ++c) {
-    if (empty(c)) continue;
-    const float2 ml = part_ml[prow + c];
-    if (!(ml.y > 0.f)) continue;
-    const float w = exp2f(ml.x - M);
-    Ls += w * ml.y;
-    const float4 o = reinterpret_cast<const float4*>(part_o + (prow + c) * HD)[lane];
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+  for (int c0 = 0; c0 < used; c0 += 4) {
+    float2 ml[4];
+    float4 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool have = c0 + u < used;
+      ml[u] = have ? part_ml[prow + c0 + u] : make_float2(-INFINITY, 0.f);
+      o[u] = have ? reinterpret_cast<const float4*>(part_o + (prow + c0 + u) * HD)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!(ml[u].y > 0.f)) continue;
+      if (ml[u].x > M) {
+        const float r = exp2f(M - ml[u].x);  // 0 while M is -inf
+        Ls *= r;
+        acc.x *= r;
+        acc.y *= r;
+        acc.z *= r;
+        acc.w *= r;
+        M = ml[u].x;
+      }
+      const float w = exp2f(ml[u].x - M);
+      Ls += w * ml[u].y;
+      acc.x += w * o[u].x;
+      acc.y += w * o[u].y;
+      acc.z += w * o[u].z;
+      acc.w += w * o[u].w;
+    }
   }
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
   const int node = grow / p.g, head = kvh * p.g + grow % p.g;
