@@ -192,9 +192,8 @@ int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
  * The pages have no counterpart to this entry point; it exists for deployment.
  *
  * Who needs it: a serving engine that hands all free HBM to its KV-cache pool at start-up
- * and allows no later cudaMalloc, a plugin whose host framework owns every device
- * allocation, or code running while a CUDA graph is captured (no cudaMalloc there).  Such
- * callers pass only inputs and outputs; the scratch comes from a 1 MiB array compiled into
+ * and allows no later cudaMalloc, or a plugin whose host framework owns every device
+ * allocation.  Such callers pass only inputs and outputs; the scratch comes from a 1 MiB array compiled into
  * the library (a file-scope __device__ array that every GPU which loads the library keeps
  * until the process exits).  No cudaMalloc, cudaFree or allocating library routine is
  * called.
@@ -205,7 +204,9 @@ int ts_tree_accept(const void* logits, ts_dtype dt, const int32_t* tokens,
  * for example B * m = 512 rows of V = 128256 use S = 2).  Larger requests return
  * TS_ERR_UNSUPPORTED without launching anything.
  * The first call on a device looks up the array's device address with that device current
- * and caches it; make that first call before any stream capture.  All calls share the one
+ * and caches it under the current CUDA context's ID (a cudaDeviceReset leads to a new
+ * context, so the next call looks it up again); make that first call before any stream
+ * capture.  All calls share the one
  * array (its previous contents are irrelevant: every slot is written before it is read), so
  * calls that may overlap on the GPU (different streams, or different host threads without
  * ordering) race and must be serialised by the caller.

@@ -13,6 +13,8 @@
 //      the parent array, mark each node valid if every node on its root path carries the
 //      argmax of its parent, pick the deepest valid node (ties -> lowest index) with a
 //      block max over a packed key, and write the path, its length and the bonus token.
+#include <cuda.h>
+
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -369,12 +371,12 @@ int tree_accept_launch(const void* logits, ts_dtype dt, const int32_t* tokens,
 //
 // Some callers cannot allocate device memory at the moment they verify a tree: a serving
 // engine that hands all free HBM to its KV-cache pool at start-up and forbids later
-// cudaMalloc calls, a plugin hosted by a framework that owns every device allocation, or
-// code that runs inside a region being captured into a CUDA graph.  This variant needs no
-// workspace from them: its scratch (the per-segment partial argmax pairs) lives in the
-// file-scope array below, which every GPU that loads this library keeps until the process
-// exits.  The device address of the array is looked up once per device, on the first call
-// made with that device current, and cached.
+// cudaMalloc calls, or a plugin hosted by a framework that owns every device allocation.
+// This variant needs no workspace from them: its scratch (the per-segment partial argmax
+// pairs) lives in the file-scope array below, which every GPU that loads this library keeps
+// until the process exits.  The device address of the array is looked up with the device
+// current on the first call made in a CUDA context (a device's first call, and the first
+// call after a cudaDeviceReset, which creates a new context), and cached with the context.
 // ---------------------------------------------------------------------------------------
 namespace {
 
@@ -384,17 +386,63 @@ __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+unsigned long long g_noalloc_ctx_id[kNoAllocMaxDevices] = {};  // 0: no address cached
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The two driver calls that name the current context, fetched once through the runtime (the
+// library links the runtime only).  A context's ID is unique for the life of the process, so
+// a context made after a reset never matches an ID cached for the one it replaced, even where
+// the driver hands back the same context handle.
+struct CtxCalls {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const CtxCalls& ctx_calls() {
+  static CtxCalls calls;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      calls.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      calls.get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  return calls;
+}
+
+// ID of the current context, 0 if the runtime has not set this thread's context up yet.
+int current_ctx_id(unsigned long long* id) {
+  const CtxCalls& c = ctx_calls();
+  if (c.get_current == nullptr || c.get_id == nullptr) return TS_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (c.get_current(&ctx) != CUDA_SUCCESS) return TS_ERR_CUDA;
+  *id = 0;
+  if (ctx != nullptr && c.get_id(ctx, id) != CUDA_SUCCESS) return TS_ERR_CUDA;
+  return TS_OK;
+}
 
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return TS_ERR_CUDA;
+  unsigned long long id = 0;
+  if (current_ctx_id(&id) != TS_OK) return TS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (id == 0 || g_noalloc_ptr[dev] == nullptr || g_noalloc_ctx_id[dev] != id) {
     // In host code the array's name is only a host-side stand-in: the kernels must get the
-    // device address, which the runtime reports for the current device.
+    // device address, which the runtime reports for the current device and context (setting
+    // the context up first if needed).
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return TS_ERR_CUDA;
+    if (current_ctx_id(&id) != TS_OK || id == 0) return TS_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx_id[dev] = id;
   }
   *out = g_noalloc_ptr[dev];
   return TS_OK;

@@ -1,11 +1,11 @@
 """ts_tree_accept_noalloc — the tree_accept variant for callers that cannot allocate.
 
 Callers such as a serving engine that gives all free device memory to its KV-cache pool,
-a plugin whose host framework owns every allocation, or code running under CUDA-graph
-capture cannot hand the library a workspace.  The no-allocation entry point keeps its
-scratch in a fixed array inside the library; these checks call it through the C ABI and
-compare it with the workspace-taking entry point on two calls in a row (outputs are
-integers, so they must agree exactly).  The file is named to be collected last.
+or a plugin whose host framework owns every allocation, cannot hand the library a
+workspace.  The no-allocation entry point keeps its scratch in a fixed array inside the
+library; these checks call it through the C ABI and compare it with the workspace-taking
+entry point on two calls in a row and at the array's exact limit (outputs are integers,
+so they must agree exactly).  The file is named to be collected last.
 """
 import ctypes
 
@@ -71,4 +71,32 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     dummy = torch.zeros(1, dtype=torch.int32, device="cuda")
     p = dummy.data_ptr()
     rc = L.ts_tree_accept_noalloc(p, TS_BF16, p, p, B, m, V, p, p, p, p, None, None)
+    assert rc == TS_ERR_UNSUPPORTED
+
+
+def test_noalloc_at_its_exact_limit():
+    """The largest request the 1 MiB array holds (131040 rows of one segment: 8 bytes each
+    plus 256 bytes of alignment) runs and matches the workspace entry point; one more row
+    is rejected."""
+    L = _lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    B, m, V = 546, 240, 2048  # 131040 rows; V = 2048 is one segment per row
+    g = torch.Generator(device="cuda").manual_seed(11)
+    logits = torch.randn(B, m, V, generator=g, device="cuda").to(torch.bfloat16)
+    parents = (torch.rand(B, m, generator=g, device="cuda") * torch.arange(m, device="cuda")).floor().to(torch.int32)
+    parents[:, 0] = -1
+    tokens = logits.float().argmax(-1).to(torch.int32).gather(1, parents.clamp(min=0).long()).to(torch.int32)
+    status_a, status_b = ts.new_status(), ts.new_status()
+    ref = ts.tree_accept(logits, tokens, parents, status=status_a)
+    got = _outs(B, m)
+    rc = L.ts_tree_accept_noalloc(logits.data_ptr(), TS_BF16, tokens.data_ptr(), parents.data_ptr(),
+                                  B, m, V, *[t.data_ptr() for t in got], status_b.data_ptr(), stream)
+    assert rc == 0, ts.status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status_a.item()) == 0 and int(status_b.item()) == 0
+    for key, t in zip(("argmax", "accept_len", "accept_path", "bonus"), got):
+        np.testing.assert_array_equal(t.cpu().numpy(), ref[key].cpu().numpy(), err_msg=key)
+    assert (got[1].cpu().numpy() > 1).any()
+    p = logits.data_ptr()
+    rc = L.ts_tree_accept_noalloc(p, TS_BF16, p, p, B, m + 1, V, p, p, p, p, None, None)
     assert rc == TS_ERR_UNSUPPORTED
