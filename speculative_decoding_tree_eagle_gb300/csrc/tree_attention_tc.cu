@@ -78,11 +78,12 @@ struct Cfg {
   static constexpr int SK = 3;  // K ring stages (K is consumed two tiles ahead of V)
   static constexpr int SV = 2;  // V ring stages
   // A TMA instruction keeps its issuing thread busy for on the order of 100 cycles, and a
-  // 128-key tile of 16-token pages is 16 boxes per operand, so each operand has several
-  // issuing warps.  Warps 0 and 3 issue K, warp 2 V; the warps after the softmax warps
-  // issue the remaining V parts, then the remaining K parts.
-  static constexpr int K_PRODUCERS = 4;
-  static constexpr int V_PRODUCERS = 2;
+  // 128-key tile of 16-token pages is 16 K boxes (2 KB) and 8 V boxes (4 KB), so K has three
+  // issuing warps: warps 0 and 3, and warp 12 after the softmax warps; warp 2 issues V (the
+  // warps after the softmax warps would take further V parts, then further K parts).  Measured
+  // on the long-context and Llama-2-70B shapes, 3 + 1 issuers beat 4 + 2 by 1-2%.
+  static constexpr int K_PRODUCERS = 3;
+  static constexpr int V_PRODUCERS = 1;
   // softmax: two threads per row (warps 4..7 the first 64 keys of a tile, warps 8..11 the
   // other 64; warp w reaches TMEM lanes 32*(w%4) .. +31), which exchange their row maxima
   // through shared memory once per tile
