@@ -125,6 +125,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // immediate) before the warp issues .sync.aligned tcgen05 instructions.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, int32_t* status) {
+  // fast path: the phase is already complete for every lane (one probe, no broadcast)
+  if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   const int lane = threadIdx.x & 31;
   int ok = 0;
   if (lane == 0) ok = mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
