@@ -99,7 +99,7 @@ struct Cfg {
   // full_k[SK] empty_k[SK] full_v[SV] empty_v[SV] s_full[2] p_full[2] o_ready o_final
   // xchg[4 quadrants][2 parities] (p_full is per S buffer: a fast softmax warp may reach tile
   // t+1 while slower warps still work on tile t, and their arrivals must not mix)
-  static constexpr int NBAR = 2 * SK + 2 * SV + 6 + 8;
+  static constexpr int NBAR = 2 * SK + 2 * SV + 6 + 8 + 1;  // + q_ready
   static constexpr uint32_t OFF_XCH = OFF_BAR + NBAR * 8;         // [2 parities][2 halves][128 rows] fp32
   static constexpr uint32_t OFF_MISC = OFF_XCH + 2 * 2 * BM * 4;
   static constexpr uint32_t OFF_ML = OFF_MISC + 16;            // (max, sum) per row, cluster merge
@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const uint32_t o_ready = bar(2 * SK + 2 * SV + 4);
   const uint32_t o_final = bar(2 * SK + 2 * SV + 5);
   auto xchg_bar = [&](int q, int par) { return bar(2 * SK + 2 * SV + 6 + 2 * q + par); };
+  const uint32_t q_ready = bar(2 * SK + 2 * SV + 14);  // Q staged by the softmax threads
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + C::OFF_MISC + 4);
 
@@ -259,37 +260,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     mbar_init(o_ready, 1);
     mbar_init(o_final, 1);
+    mbar_init(q_ready, 64 * nact);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
     tmem_relinquish();
-  }
-  // Q rows of this row group -> shared memory in the 128-byte-swizzled K-major layout
-  // (16-byte chunk j of row r stored at chunk j ^ (r % 8)); padding rows are zero.  Loads
-  // are issued in batches of 4 per thread so their latencies overlap.
-  for (int c0 = threadIdx.x; c0 < BM * 16; c0 += 4 * C::THREADS) {
-    uint4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * C::THREADS;
-      const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (nt > 0 && c < BM * 16 && row < rows_here) {
-        const int grow = R0 + row;
-        const int node = grow / p.g, head = kvh * p.g + grow % p.g;
-        const long long off = ((static_cast<long long>(b) * p.m + node) * p.Hq + head) * HD + h * 64 + j * 8;
-        v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + off));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * C::THREADS;
-      if (c >= BM * 16) break;
-      const int row = c >> 4, h = (c >> 3) & 1, j = c & 7;
-      *reinterpret_cast<uint4*>(sptr + C::OFF_Q + h * QHALF + row * 128 + ((j ^ (row & 7)) << 4)) = v[u];
-    }
   }
   // Physical block of every TMA box row group of this chunk -> shared memory (warp 0,
   // coalesced, 4 independent loads in flight per lane); out-of-range ids are reported and
@@ -436,7 +413,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           mma_ts(tmem, tP(sb) + 8u * kk, vdesc[kk] + static_cast<uint64_t>(sv * (KTILE >> 4)), idp,
                  (first && kk == 0) ? 0u : 1u);
       };
-      bool mok = true;
+      bool mok = mbar_wait(q_ready, 0, abort_flag, p.status);
       for (int t = 0; mok && t < 2 && t < nt; ++t) {
         mok = mbar_wait(full_k(t % SK), (t / SK) & 1, abort_flag, p.status);
         if (!mok) break;
@@ -489,6 +466,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t tO = tmem + lane_off + 64u * hh;
+      {  // this row's head-dim half hh of Q -> shared memory in the 128-byte-swizzled K-major
+         // layout (16-byte chunk j of row r at chunk j ^ (r % 8)); zeros for padding rows.  The
+         // softmax threads stage Q after the CTA's set-up, while the producers start loading.
+        const long long qoff =
+            ((static_cast<long long>(b) * p.m + node) * p.Hq + kvh * p.g + (valid ? grow % p.g : 0)) * HD + 64 * hh;
+        uint4 qv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          qv[j] = valid ? __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(sptr + C::OFF_Q + hh * QHALF + r * 128 + ((j ^ (r & 7)) << 4)) = qv[j];
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+      }
       const float sl2 = p.scale_log2;
       float* xch = reinterpret_cast<float*>(sptr + C::OFF_XCH);
       // the partner thread's value for exchange round `round` (both threads of a row take part
