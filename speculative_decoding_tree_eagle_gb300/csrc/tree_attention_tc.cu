@@ -26,7 +26,9 @@
 //                        P V of tile t, so the tensor cores work while the softmax of tile t+1
 //                        runs.
 //   warps 4..11          softmax, two threads per row (TMEM lane): warps 4..7 take keys 0..63
-//                        of every tile, warps 8..11 keys 64..127.  Each loads its 64 scores,
+//                        of every tile, warps 8..11 keys 64..127.  First each stages its row's
+//                        head-dim half of Q in shared memory (the MMA thread waits for all of
+//                        them on an mbarrier).  Per tile each loads its 64 scores,
 //                        applies the tree mask on the tiles that reach the tree, exchanges its
 //                        row maximum with its partner through shared memory, and runs the
 //                        online softmax in the log2 domain with lazy rescaling of its half of O
