@@ -90,7 +90,9 @@ struct Cfg {
   // other 64; warp w reaches TMEM lanes 32*(w%4) .. +31), which exchange their row maxima
   // through shared memory once per tile
   static constexpr int EXTRA_WARP = 12;
-  static constexpr int THREADS = 32 * (EXTRA_WARP + (K_PRODUCERS - 2) + (V_PRODUCERS - 1));
+  // the P V issuer has a warp of its own after the extra producers (warp 1 issues Q K^T)
+  static constexpr int PV_WARP = EXTRA_WARP + (K_PRODUCERS - 2) + (V_PRODUCERS - 1);
+  static constexpr int THREADS = 32 * (PV_WARP + 1);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 128;
   static constexpr uint32_t COL_P = 384;
@@ -101,7 +103,8 @@ struct Cfg {
   // full_k[SK] empty_k[SK] full_v[SV] empty_v[SV] s_full[2] p_full[2] o_ready o_final
   // xchg[4 quadrants][2 parities] (p_full is per S buffer: a fast softmax warp may reach tile
   // t+1 while slower warps still work on tile t, and their arrivals must not mix)
-  static constexpr int NBAR = 2 * SK + 2 * SV + 6 + 8 + 1;  // + q_ready
+  // + q_ready, p_free[2] (P V has read that P buffer), qk_done
+  static constexpr int NBAR = 2 * SK + 2 * SV + 6 + 8 + 1 + 3;
   static constexpr uint32_t OFF_XCH = OFF_BAR + NBAR * 8;         // [2 parities][2 halves][128 rows] fp32
   static constexpr uint32_t OFF_MISC = OFF_XCH + 2 * 2 * BM * 4;
   static constexpr uint32_t OFF_ML = OFF_MISC + 16;            // (max, sum) per row, cluster merge
@@ -124,6 +127,7 @@ struct Params {
   int32_t* status;
   int B, m, Hq, Hkv, g, rows, W, max_blocks, num_blocks, block_size, max_prefix, tpc, nchunk, mode;
   int mc;  // row groups sharing each K/V tile through TMA multicast (a cluster along x), 1 = none
+  int split_issue;  // 1: Q K^T and P V issued by two threads (warp 1, PV_WARP); 0: warp 1 issues both
   float scale_log2;
 };
 
@@ -240,6 +244,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const uint32_t o_final = bar(2 * SK + 2 * SV + 5);
   auto xchg_bar = [&](int q, int par) { return bar(2 * SK + 2 * SV + 6 + 2 * q + par); };
   const uint32_t q_ready = bar(2 * SK + 2 * SV + 14);  // Q staged by the softmax threads
+  auto p_free = [&](int sb) { return bar(2 * SK + 2 * SV + 15 + sb); };
+  const uint32_t qk_done = bar(2 * SK + 2 * SV + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sptr + C::OFF_MISC + 4);
 
@@ -263,6 +269,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(o_ready, 1);
     mbar_init(o_final, 1);
     mbar_init(q_ready, 64 * nact);
+    mbar_init(p_free(0), 1);
+    mbar_init(p_free(1), 1);
+    mbar_init(qk_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   float m_ref = -INFINITY, l_sum = 0.f;
   bool ok = true;
 
-  if (warp == 0 || warp == 2 || warp == 3 || warp >= C::EXTRA_WARP) {
+  if (warp == 0 || warp == 2 || warp == 3 || (warp >= C::EXTRA_WARP && warp < C::PV_WARP)) {
     // ------------------------------ TMA producers ------------------------------
     // Part `part` of `nparts` issues boxes [part*nbox/nparts, (part+1)*nbox/nparts) of every
     // tile (a part may hold none: it still registers its zero bytes once per tile).
@@ -382,26 +391,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0 && nt > 0) {
+    // ------------------------------ MMA issue ------------------------------
+    // With several row groups (split_issue) warp 1 issues only Q K^T and the P V issuer warp
+    // P V, so neither waits behind the other's barrier; with one row group warp 1 issues both.
+    // Split: S_t = Q K_t^T (M=128, N=128, K=128; A, B from shared memory) into S buffer t%2, once K_t
+    // is in and the softmax is done with the buffer's previous tile (its p_full: it has read S
+    // and written P)
+    if (lane == 0 && nt > 0 && !p.split_issue) {
+      // one thread issues both: S_t = Q K_t^T and O += P_t V_t; S and P are double-buffered, Q K^T
+      // of tile t+2 is issued right after P V of tile t (in issue order, so P V has read P before
+      // the softmax of tile t+2 rewrites it), and the tensor cores work while the softmax of
+      // tile t+1 runs
       constexpr uint32_t idq = idesc_bf16_f32(128, BN, 0, 0);
       constexpr uint32_t idp = idesc_bf16_f32(128, HD, 0, 1);
-      auto tS = [&](int sb) { return tmem + C::COL_S + 128u * sb; };
-      auto tP = [&](int sb) { return tmem + C::COL_P + 64u * sb; };
       auto qk = [&](int sk, int sb) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t h = kk >> 2, ko = (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + h * QHALF + ko, 16, 1024);
           const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + sk * KTILE + h * KHALF + ko, 16, 1024);
-          mma_ss(tS(sb), a, bd, idq, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_S + 128u * sb, a, bd, idq, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full(sb));
       };
-      // B = V keys 16kk .. 16kk+15, MN-major: 64 head-dim columns per 128-byte row, 8-key
-      // groups 1 KB apart (stride offset), the second head-dim half rpb*128 further (leading
-      // offset); the keys sit in box row (16kk)/rpb at row (16kk)%rpb.  Descriptors of stage 0;
-      // a stage adds KTILE (in 16-byte units) to the start address field.
       uint64_t vdesc[BN / 16];
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
@@ -412,7 +424,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       auto pv = [&](int sv, int sb, bool first) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem, tP(sb) + 8u * kk, vdesc[kk] + static_cast<uint64_t>(sv * (KTILE >> 4)), idp,
+          mma_ts(tmem, tmem + C::COL_P + 64u * sb + 8u * kk, vdesc[kk] + static_cast<uint64_t>(sv * (KTILE >> 4)), idp,
                  (first && kk == 0) ? 0u : 1u);
       };
       bool mok = mbar_wait(q_ready, 0, abort_flag, p.status);
@@ -444,6 +456,71 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (mc > 1) tc_commit_mc(empty_k(tn % SK), mc_mask);
           else tc_commit(empty_k(tn % SK));
         }
+      }
+      tc_commit(o_final);
+      if (!mok) drain_wait(o_final, 0);
+    }
+    if (lane == 0 && nt > 0 && p.split_issue) {
+      constexpr uint32_t idq = idesc_bf16_f32(128, BN, 0, 0);
+      bool mok = mbar_wait(q_ready, 0, abort_flag, p.status);
+      for (int t = 0; mok && t < nt; ++t) {
+        const int sb = t & 1, sk = t % SK;
+        if (t >= 2) {
+          mok = mbar_wait(p_full(sb), ((t - 2) >> 1) & 1, abort_flag, p.status);
+          if (!mok) break;
+        }
+        mok = mbar_wait(full_k(sk), (t / SK) & 1, abort_flag, p.status);
+        if (!mok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t h = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + h * QHALF + ko, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + sk * KTILE + h * KHALF + ko, 16, 1024);
+          mma_ss(tmem + C::COL_S + 128u * sb, a, bd, idq, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(sb));
+        if (mc > 1) tc_commit_mc(empty_k(sk), mc_mask);
+        else tc_commit(empty_k(sk));
+      }
+      tc_commit(qk_done);
+      if (!mok) drain_wait(qk_done, 0);
+    }
+    __syncwarp();
+  } else if (warp == C::PV_WARP && p.split_issue) {
+    // ------------------------------ P V issuer ------------------------------
+    // O += P_t V_t (M=128, N=128, K=128; A = P from TMEM, B = V MN-major) once V_t and P_t are
+    // in; its commits tell the softmax that O holds this tile (o_ready) and that the P buffer
+    // may be rewritten (p_free)
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idp = idesc_bf16_f32(128, HD, 0, 1);
+      // B = V keys 16kk .. 16kk+15, MN-major: 64 head-dim columns per 128-byte row, 8-key
+      // groups 1 KB apart (stride offset), the second head-dim half rpb*128 further (leading
+      // offset); the keys sit in box row (16kk)/rpb at row (16kk)%rpb.  Descriptors of stage 0;
+      // a stage adds KTILE (in 16-byte units) to the start address field.
+      uint64_t vdesc[BN / 16];
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const int key = 16 * kk;
+        const uint32_t off = (key / rpb) * rpb * 256 + (key % rpb) * 128;
+        vdesc[kk] = sdesc_sw128(sbase + C::OFF_V + off, rpb * 128, 1024);
+      }
+      bool mok = true;
+      for (int t = 0; mok && t < nt; ++t) {
+        const int sv = t % SV, sb = t & 1;
+        mok = mbar_wait(full_v(sv), (t / SV) & 1, abort_flag, p.status);
+        if (!mok) break;
+        mok = mbar_wait(p_full(sb), (t >> 1) & 1, abort_flag, p.status);
+        if (!mok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem, tmem + C::COL_P + 64u * sb + 8u * kk, vdesc[kk] + static_cast<uint64_t>(sv * (KTILE >> 4)),
+                 idp, (t == 0 && kk == 0) ? 0u : 1u);
+        tc_commit(o_ready);
+        tc_commit(p_free(sb));
+        if (mc > 1) tc_commit_mc(empty_v(sv), mc_mask);
+        else tc_commit(empty_v(sv));
       }
       tc_commit(o_final);
       if (!mok) drain_wait(o_final, 0);
@@ -553,6 +630,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const float p1 = ex2_approx(x1);
             rs4[c & 3] += p0 + p1;
             pk[c] = pack_bf16x2(p0, p1);
+          }
+          if (p.split_issue && t >= 2) {  // P V of tile t-2 has read this P buffer
+            ok = mbar_wait_warp(p_free(sb), ((t >> 1) - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
           }
           tmem_st32(tP, pk);
           l_sum += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
@@ -1137,6 +1219,13 @@ int attention_tc_launch(const AttnArgs& a, int num_sms) {
   prm.nchunk = pl.nc;
   prm.mode = pl.mode;
   prm.mc = pl.mc;
+  // two MMA-issuing threads pay off where the tensor cores set the pace (several row groups);
+  // with one row group the single issuer is 2% faster
+  prm.split_issue = pl.rowgroups >= 2 ? 1 : 0;
+  if (const char* ov = std::getenv("TREESPEC_ATTN_ISSUE")) {
+    if (std::strcmp(ov, "1") == 0) prm.split_issue = 0;
+    else if (std::strcmp(ov, "2") == 0) prm.split_issue = 1;
+  }
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   const size_t prow = static_cast<size_t>(a.B) * a.Hkv * prm.rows * pl.nc;
   prm.part_o = pl.mode == tc::kGlobal ? static_cast<float*>(a.workspace) : nullptr;

@@ -232,3 +232,31 @@ def test_ragged_batch_longest_first(split, monkeypatch):
     lens = inp["prefix_len"].tolist()
     assert max(lens) - min(lens) > 1000, lens
     _run(inp, w, tree["mask"], tree["mask_words"])
+
+
+@pytest.mark.parametrize("split", ["direct", "cluster:2", "global:3"])
+@pytest.mark.parametrize("cfg", [dict(B=2, Hq=8, Hkv=2, prefix=(1500, 2300), m=30, k=5, depth=6),    # 1 row group
+                                 dict(B=2, Hq=32, Hkv=8, prefix=(900, 2100), m=64, k=10, depth=7),   # 2 row groups
+                                 dict(B=2, Hq=64, Hkv=8, prefix=(700, 1500), m=60, k=8, depth=6)],   # 4 row groups
+                         ids=["1_group", "2_groups", "4_groups"])
+def test_one_and_two_mma_issuers_agree(cfg, split, monkeypatch):
+    """Q K^T and P V issued by one thread (in issue order) or by two threads (each gated by its
+    barriers, the softmax waiting until P V has read a P buffer before rewriting it): the same
+    MMAs in the same order per accumulator, so the outputs and log-sum-exps are bit-identical,
+    and both match the oracle."""
+    lib()
+    monkeypatch.setenv("TREESPEC_ATTN_SPLIT", split)
+    w, inp, tree = _small("attn_issue", **cfg)
+    g = {k: inp[k].to(dev()) for k in ("q", "k_cache", "v_cache", "block_table", "prefix_len")}
+    outs = []
+    for issue in ("1", "2"):
+        monkeypatch.setenv("TREESPEC_ATTN_ISSUE", issue)
+        status = ts.new_status(dev())
+        out, lse = ts.tree_attention(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["prefix_len"],
+                                     words_i64(tree["mask_words"]), max_prefix=w.max_prefix, status=status)
+        ts.check_status(status)
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ref, _ = oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"].numpy(),
+                                   inp["prefix_len"].numpy(), tree["mask"], scale_of(w))
+    assert_attention_close(outs[1][0], ref, torch.bfloat16)
