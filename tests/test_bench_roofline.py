@@ -28,3 +28,31 @@ def test_fraction_is_achieved_over_peak_in_the_chosen_unit():
     r = bench.attention_roofline(1e8, 1e12, 1.0, HBM, TENSOR, None)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["achieved"] == 1000.0
     assert r["frac"] == round(1000.0 / 1872.8, 4) and r["peak"] == 1872.8
+
+
+def test_algorithmic_bytes_are_the_documented_per_unit_counts():
+    """The roofline's numerator, counted by hand from the per-unit figures: each input byte read
+    once, each output byte written once (Llama-2-7B shape: B 1, 51 draft rows of 32000 fp32,
+    m 60, 32 heads of 128, 2048-token prefix in 16-token pages; long-context m64: B 4, 71 rows
+    of 128256, m 64, 32/8 heads, 32768-token prefixes)."""
+    w = workloads.WORKLOADS["llama2_7b"]
+    b = bench.algo_bytes(w, [2048])
+    # draft rows in, root token in; tokens/parents/depth int32, one mask word, fp64 value out
+    assert b["tree_build"] == 51 * 32000 * 4 + 4 + 60 * (3 * 4 + 8 + 8)
+    # K and V of prefix + tree, Q and out, one mask word per node, 132 page ids, the prefix
+    # length, the fp32 log-sum-exp per (node, head)
+    assert b["tree_attention"] == ((2048 + 60) * 32 * 128 * 2 * 2 + 2 * 60 * 32 * 128 * 2 + 60 * 8
+                                   + 132 * 4 + 4 + 60 * 32 * 4)
+    # bf16 logits, tokens + parents in; argmax + path out; length + bonus out
+    assert b["tree_accept"] == 60 * 32000 * 2 + 60 * 8 + 60 * 8 + 8
+    assert b["step"] == b["tree_build"] + b["tree_attention"] + b["tree_accept"] == 45899856
+
+    w = workloads.WORKLOADS["long_context_m64"]
+    lens = [32768] * 4
+    b = bench.algo_bytes(w, lens)
+    assert b["tree_build"] == 4 * 71 * 128256 * 4 + 4 * 4 + 4 * 64 * (3 * 4 + 8 + 8)
+    assert b["tree_attention"] == 4 * ((32768 + 64) * 8 * 128 * 2 * 2 + 2 * 64 * 32 * 128 * 2 + 64 * 8
+                                       + 2052 * 4 + 4 + 64 * 32 * 4)
+    assert b["tree_accept"] == 4 * (64 * 128256 * 2 + 64 * 8 + 64 * 8 + 8)
+    # 4 d FLOPs per (query row, prefix key): two d-long dot products, multiply and add
+    assert bench.attention_flops(w, lens) == 4 * 128 * (64 * 32) * (4 * 32768)
