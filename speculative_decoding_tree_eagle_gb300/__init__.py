@@ -9,6 +9,12 @@ without a CUDA device, every call raises.
     tree_build(draft_logp, root_tokens, k, depth, m)      -> dict(tokens, parents, depth, mask, values)
     tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, ...) -> (out, lse)
     tree_accept(logits, tokens, parents)                  -> dict(argmax, accept_len, accept_path, bonus)
+
+The rows after the path: ``kv_commit`` (keep the accepted path's K/V rows, release the
+rejected pages), ``lm_head_argmax`` / ``tree_accept_hidden`` (target LM head with the argmax in
+its GEMM epilogue), ``efficient_head`` / ``tree_build_from_topk`` (the draft's two-stage head
+and the tree from its lists), ``tree_accept_sample`` (acceptance at temperature T > 0) and
+``tree_prune`` (cost-aware pruning before verification).
 """
 from __future__ import annotations
 
@@ -23,7 +29,7 @@ import torch
 __all__ = [
     "TreeSpecError", "library", "library_path", "launch_count", "status_string",
     "tree_build", "tree_attention", "tree_accept", "kv_commit", "lm_head_argmax", "tree_accept_hidden",
-    "efficient_head", "tree_build_from_topk",
+    "efficient_head", "tree_build_from_topk", "tree_accept_sample", "tree_prune",
     "new_status", "check_status",
     "tree_build_workspace", "tree_attention_workspace", "tree_accept_workspace", "tree_attention_plan",
 ]

@@ -169,3 +169,18 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         ts.tree_accept(torch.zeros(1, 2, 4), torch.zeros(1, 2, dtype=torch.int32),
                        torch.zeros(1, 2, dtype=torch.int32))
+
+
+def test_binding_covers_every_public_call(lib):
+    """Every public name of the binding exists, and each public library call of the header
+    that a Python user needs has a binding function of the same name without the ts_ prefix
+    (the self-test, version, status, launch-count, plan, workspace and no-allocation entry
+    points are reached through ``library()``)."""
+    for name in ts.__all__:
+        assert hasattr(ts, name), name
+    internal = ("ts_selftest_", "ts_version", "ts_status_string", "ts_launch_count", "_workspace",
+                "ts_tree_accept_noalloc", "ts_efficient_head_candidates", "ts_tree_attention_plan")
+    for sym in declared_symbols():
+        if any(part in sym for part in internal):
+            continue
+        assert sym[3:] in ts.__all__, sym
