@@ -160,6 +160,15 @@ int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, t
 int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
                            int block_size, int* plan_out);
 
+/* The same plan for a GPU with num_sms streaming multiprocessors in place of the current
+ * device's count (sizing ahead of time, or for a share of the SMs; 152 on a GB300).  The row
+ * groups, chunks and tiles per chunk follow from the sizes and num_sms alone; multicast and
+ * the in-cluster merge are chosen only where the current device reports that it can
+ * co-schedule such clusters, so with no device present the plan uses neither.
+ * num_sms < 1 -> TS_ERR_INVALID; otherwise as ts_tree_attention_plan. */
+int ts_tree_attention_plan_for_sms(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                                   int block_size, int num_sms, int* plan_out);
+
 /* ------------------------------------------------------------------------------------
  * ts_tree_accept — greedy verification of the tree.
  * Source: "lesty.tech — EAGLE-2 vs. Medusa", section 4 (greedy: a draft token is accepted iff

@@ -73,6 +73,8 @@ def library():
         L.ts_tree_attention.argtypes = [P, P, P, I, I, I, P, I, P, I, P, I, I, I, I, I, F, P, P, P, S, P, P]
         L.ts_tree_attention_plan.restype = I
         L.ts_tree_attention_plan.argtypes = [I, I, I, I, I, I, I, I, P]
+        L.ts_tree_attention_plan_for_sms.restype = I
+        L.ts_tree_attention_plan_for_sms.argtypes = [I, I, I, I, I, I, I, I, I, P]
         L.ts_tree_accept_workspace.restype = S
         L.ts_tree_accept_workspace.argtypes = [I, I, I, I]
         L.ts_tree_accept.restype = I
@@ -188,11 +190,17 @@ def tree_attention_workspace(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: i
 
 
 def tree_attention_plan(dtype: torch.dtype, B: int, m: int, Hq: int, Hkv: int, d: int, max_prefix: int,
-                        block_size: int) -> Dict[str, int]:
-    """The launch plan tree_attention uses for these sizes on the current device."""
+                        block_size: int, num_sms: Optional[int] = None) -> Dict[str, int]:
+    """The launch plan tree_attention uses for these sizes on the current device, or, with
+    ``num_sms``, for that many SMs (multicast and the in-cluster merge still depend on what the
+    current device can co-schedule; with no device present neither is chosen)."""
     dt = TS_F32 if dtype == torch.float32 else TS_BF16
     out = (ctypes.c_int * 6)()
-    _check(library().ts_tree_attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, out))
+    if num_sms is None:
+        _check(library().ts_tree_attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, out))
+    else:
+        _check(library().ts_tree_attention_plan_for_sms(dt, B, m, Hq, Hkv, d, max_prefix, block_size,
+                                                        int(num_sms), out))
     modes = {0: "one chunk", 1: "cluster merge", 2: "workspace merge"}
     return {"path": "tensor-core" if out[0] else "cuda-core", "row_groups": out[1], "chunks": out[2],
             "tiles_per_chunk": out[3], "split": modes.get(out[4], str(out[4])), "multicast": out[5]}

@@ -101,8 +101,9 @@ size_t ts_tree_attention_workspace(ts_dtype dt, int B, int m, int Hq, int Hkv, i
   return 256;
 }
 
-int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
-                           int block_size, int* plan_out) {
+// num_sms <= 0: the current device's SM count, looked up only for the tensor-core path
+static int attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                          int block_size, int num_sms, int* plan_out) {
   const int rc = ts::check_attention(dt, B, m, Hq, Hkv, d, max_prefix);
   if (rc != TS_OK) return rc;
   if (!plan_out || block_size <= 0) return TS_ERR_INVALID;
@@ -116,8 +117,19 @@ int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, in
     return TS_OK;
   }
   plan_out[0] = 1;
-  ts::attention_tc_plan(B, m, Hq, Hkv, max_prefix, ts::device_sm_count(), plan_out + 1);
+  ts::attention_tc_plan(B, m, Hq, Hkv, max_prefix, num_sms > 0 ? num_sms : ts::device_sm_count(), plan_out + 1);
   return TS_OK;
+}
+
+int ts_tree_attention_plan(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                           int block_size, int* plan_out) {
+  return attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, 0, plan_out);
+}
+
+int ts_tree_attention_plan_for_sms(ts_dtype dt, int B, int m, int Hq, int Hkv, int d, int max_prefix,
+                                   int block_size, int num_sms, int* plan_out) {
+  if (num_sms < 1) return TS_ERR_INVALID;
+  return attention_plan(dt, B, m, Hq, Hkv, d, max_prefix, block_size, num_sms, plan_out);
 }
 
 int ts_tree_attention(const void* q, const void* k_cache, const void* v_cache, ts_dtype dt,

@@ -184,3 +184,39 @@ def test_binding_covers_every_public_call(lib):
         if any(part in sym for part in internal):
             continue
         assert sym[3:] in ts.__all__, sym
+
+
+@pytest.mark.parametrize("name,row_groups,chunks,tiles", [
+    ("llama2_7b", 1, 4, 5),            # 2108 keys = 17 tiles; 32 units on 152 SMs
+    ("llama3_8b_gqa", 2, 2, 33),       # one chunk would leave SMs idle: split in two halves
+    ("llama2_70b_gqa", 4, 1, 33),      # 512 CTAs already fill several waves
+    ("long_context_m8", 1, 4, 65),     # 257 tiles over 4 chunks
+    ("long_context_m32", 1, 4, 65),
+    ("long_context_m64", 2, 2, 129),
+    ("long_context_m128", 4, 2, 129),
+])
+def test_attention_plan_on_a_gb300(lib, name, row_groups, chunks, tiles, monkeypatch):
+    """The planner's split of each workload for 152 SMs: row groups of 128 GEMM rows
+    (node x head in group), chunks per (sequence, KV head, row group) and tiles per chunk."""
+    import torch
+    import workloads
+    for var in ("TREESPEC_ATTN_SPLIT", "TREESPEC_ATTN_MC", "TREESPEC_ATTN_ISSUE"):
+        monkeypatch.delenv(var, raising=False)
+    w = workloads.WORKLOADS[name]
+    plan = ts.tree_attention_plan(torch.bfloat16, w.B, w.m, w.Hq, w.Hkv, w.d, w.max_prefix, 16, num_sms=152)
+    assert plan["path"] == "tensor-core"
+    assert (plan["row_groups"], plan["chunks"], plan["tiles_per_chunk"]) == (row_groups, chunks, tiles)
+    assert plan["row_groups"] == -(-w.m * (w.Hq // w.Hkv) // 128)
+    assert plan["chunks"] * plan["tiles_per_chunk"] >= -(-(w.max_prefix + w.m) // 128)
+    assert (plan["split"] == "one chunk") == (plan["chunks"] == 1)
+
+
+def test_attention_plan_paths_and_validation(lib):
+    import torch
+    # fp32 and d = 64 take the CUDA-core kernel; no SM count is needed for them
+    assert ts.tree_attention_plan(torch.float32, 1, 8, 1, 1, 64, 16, 16, num_sms=152)["path"] == "cuda-core"
+    assert ts.tree_attention_plan(torch.bfloat16, 1, 8, 4, 1, 64, 16, 16, num_sms=152)["path"] == "cuda-core"
+    out = (ctypes.c_int * 6)()
+    assert lib.ts_tree_attention_plan_for_sms(1, 1, 8, 4, 1, 128, 64, 16, 0, out) == TS_ERR_INVALID
+    assert lib.ts_tree_attention_plan_for_sms(1, 1, 8, 6, 4, 128, 64, 16, 152, out) == TS_ERR_INVALID
+    assert lib.ts_tree_attention_plan_for_sms(1, 1, 8, 4, 1, 128, 64, 16, 152, None) == TS_ERR_INVALID
