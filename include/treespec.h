@@ -25,8 +25,12 @@
  *     `*dev_status` (an int32 device word, may be NULL to ignore) and the affected work is
  *     skipped.  Kernels never trap.  The caller zeroes *dev_status and reads it after the
  *     stream has synchronised.
- *   - The library keeps no state between calls and is safe to call from several host
- *     threads.  Calls that share a workspace must be ordered on one stream.
+ *   - The library keeps no state that affects results and is safe to call from several
+ *     host threads.  It caches launch set-up per process, under locks: kernel attributes,
+ *     cluster occupancy and encoded K/V tensor maps (filled by the first calls, which
+ *     should come before any stream capture) and the no-allocation scratch address.  The
+ *     attribute and occupancy caches assume one GPU model per process; the tested use is
+ *     one process per GPU.  Calls that share a workspace must be ordered on one stream.
  *
  * Notation: B sequences, m tree nodes per sequence INCLUDING the root (node 0), k draft
  * top-k, depth draft layers below the root, V vocabulary, Hq query heads, Hkv KV heads
