@@ -56,3 +56,28 @@ def test_algorithmic_bytes_are_the_documented_per_unit_counts():
     assert b["tree_accept"] == 4 * (64 * 128256 * 2 + 64 * 8 + 64 * 8 + 8)
     # 4 d FLOPs per (query row, prefix key): two d-long dot products, multiply and add
     assert bench.attention_flops(w, lens) == 4 * 128 * (64 * 32) * (4 * 32768)
+
+
+def test_reference_arm_line_has_the_contract_keys_and_our_config():
+    """One process, the tiny workload: the reference arm (the fp64 oracle on the host) prints
+    one JSON line with the contract's keys, and its ``config`` is the object the GPU arm
+    prints for the same arguments."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    argv = ["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + argv, capture_output=True,
+                       text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["value"] > 0
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"] == bench.config_of("tiny", bench.parse(argv), 1)
