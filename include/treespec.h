@@ -306,6 +306,9 @@ int ts_efficient_head(const void* hidden, const void* lr_b, const void* lr_a, co
  * descending, ties -> lower token; a row out of order sets *dev_status to
  * TS_ERR_DEVICE_CHECK and the sequence's outputs are not written).  Expansion, rerank,
  * flatten and mask as ts_tree_build.  One launch; no workspace.
+ * Sources: "jialefu.github.io — EAGLE-4 efficient LM head", section "EAGLE Efficient LM Head"
+ * (the draft head hands on only its top candidates per position); "rainlin.net/posts/eagle",
+ * sections 7.1-7.2 (expansion and rerank over those candidates).
  */
 int ts_tree_build_from_topk(const int32_t* row_tok, const float* row_logp, const int32_t* root_tokens,
                             int B, int k, int depth, int m, int32_t* tokens, int32_t* parents,
